@@ -1,0 +1,35 @@
+"""CPU fp64 oracle for the packed varlen attention hot path -- TEST INFRASTRUCTURE ONLY.
+
+This package is the plain, slow, obviously-correct statement of what the GPU path computes.
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import it.  The product library never routes through it, and it shares no code, table or
+helper with the CUDA sources.
+
+Sources (page title + section):
+  [H3-vLLM]  "Joint audio/video generation in production: MiniMax-H3 and vLLM-Omni"
+             §3 "Packed sequence and modality identity" (modality tags choose the RoPE
+             treatment; cu_seqlens restrict softmax to the own sub-sequence; the worked
+             example [0,10,30] -> [0,10,30,45]);
+             §6 "Boundary trim of packed attention" (only the valid length enters the kernel).
+  [H3-fast]  "Breaking the engineering bottlenecks of video-generation models"
+             "Crossing the time boundary", step 3 "RoPE global time alignment"
+             (t_global = t_local + s*40/24, time axis only, decimals kept);
+             "Breaking the memory wall: window attention across GPUs" (regular and half-shifted
+             3D windows, edge windows cropped, token order restored afterwards).
+
+Every function here is pinned by tests/test_oracle_pins.py against closed forms, textbook
+routines, brute force and the pages' printed examples.  Readings where the pages are silent
+are listed in the module docstrings of ``rope`` and ``window``.
+"""
+from .attention import varlen_attention, attention_weights, dense_masked_attention_bruteforce
+from .rope import (continuation_time_shift, rope_inv_freq, rope_angles, rope_apply,
+                   video_axis_split)
+from .window import (axis_window_count, window_count, window_ids, window_partition,
+                     window_pack, window_unpack)
+
+__all__ = [
+    "varlen_attention", "attention_weights", "dense_masked_attention_bruteforce",
+    "continuation_time_shift", "rope_inv_freq", "rope_angles", "rope_apply", "video_axis_split",
+    "axis_window_count", "window_count", "window_ids", "window_partition", "window_pack",
+    "window_unpack",
+]
