@@ -1,0 +1,192 @@
+/*
+ * h3attn -- packed varlen attention with modality-tagged 3D RoPE, for GB300 (sm_103a).
+ *
+ * C ABI.  Plain pointers and sizes only.  Every buffer is owned by the caller; the library
+ * allocates no device memory except one 4-byte error word per device (a static __device__
+ * variable), and keeps no state between calls except cached driver entry points.
+ *
+ * Sources (page title + section):
+ *   [H3-vLLM] "Joint audio/video generation in production: MiniMax-H3 and vLLM-Omni"
+ *       sec. 3 "Packed sequence and modality identity": one packed 1-D sequence of text,
+ *       audio and video rows; cu_seqlens holds the sub-sequence offsets; the kernel makes each
+ *       sub-sequence softmax over its own keys only (worked example [0,10,30] -> [0,10,30,45]);
+ *       a per-token modality tag selects the RoPE treatment.
+ *       sec. 6 "Boundary trim of packed attention": only the valid length (58,758 of an aligned
+ *       58,816) may enter the kernel; the trim changes a length and a pointer, copies nothing.
+ *   [H3-fast] "Breaking the engineering bottlenecks of video-generation models"
+ *       "Crossing the time boundary", step 3: t_global = t_local + s * 40/24 before RoPE,
+ *       time axis only, decimals kept.
+ *       "Breaking the memory wall: window attention across GPUs": regular and half-shifted
+ *       3D windows with cropped edge windows; tokens gathered per window, order restored.
+ *
+ * Conventions for every call:
+ *   - Tensors Q, K, V, O are bf16, row-major [C, H, D]: token stride H*D elements, D contiguous.
+ *     C (capacity) >= N (valid tokens) -- rows in [N, C) are padding: never read as keys or
+ *     values that contribute, never written.
+ *   - Device pointers must be 16-byte aligned; head_dim must be 64 or 128.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).  They
+ *     return after host-side validation of scalars and pointers.  A status other than H3_OK
+ *     means nothing was launched.
+ *   - Device-side contents (cu_seqlens, perm) are checked by the kernels: a bad value makes
+ *     the kernel skip the affected work and record an error code in the device error word,
+ *     never access memory out of bounds.  h3_get_device_error() reads (and clears) that word.
+ *   - No exceptions cross the ABI; nothing aborts; no device trap.
+ */
+#ifndef H3ATTN_H_
+#define H3ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define H3_API __attribute__((visibility("default")))
+#else
+#define H3_API
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* h3_stream_t;
+
+typedef enum {
+  H3_OK = 0,
+  H3_ERR_NULL = 1,            /* a required pointer is NULL */
+  H3_ERR_INVALID_ARG = 2,     /* a size or scalar is out of range */
+  H3_ERR_BAD_CU_SEQLENS = 3,  /* (device) cu_seqlens not 0-based, decreasing, beyond capacity,
+                                 or a segment longer than max_seqlen */
+  H3_ERR_UNSUPPORTED = 4,     /* head_dim not in {64, 128}, or no sm_103a device */
+  H3_ERR_WORKSPACE = 5,       /* workspace missing or too small */
+  H3_ERR_CUDA = 6,            /* a CUDA runtime / driver call failed */
+  H3_ERR_TIMEOUT = 7,         /* (device) a bounded wait inside a kernel ran out */
+  H3_ERR_MISALIGNED = 8,      /* a device pointer or row size is not 16-byte aligned */
+  H3_ERR_BAD_PERM = 9         /* (device) a permutation entry is out of range */
+} h3_status;
+
+enum { H3_TAG_TEXT = 0, H3_TAG_VIDEO = 1, H3_TAG_AUDIO = 2 };
+
+/* RoPE configuration ([H3-vLLM] sec. 3: the tag selects the frequencies).
+ * Zero / negative fields select the defaults given in brackets. */
+typedef struct {
+  float base_text;      /* [10000] ladder base of text rows: one band over all D dims, by t */
+  float base_video;     /* [10000] ladder base of each video band */
+  float base_audio;     /* [10000] ladder base of audio rows: one band over all D dims, by t */
+  int32_t video_dims_t; /* video band widths, must sum to head_dim and be even;   */
+  int32_t video_dims_h; /*   all three 0 selects D/2 : D/4 : D/4                   */
+  int32_t video_dims_w; /*   (32/16/16 at D = 64, 64/32/32 at D = 128)           */
+  float audio_hz;       /* [40] numerator of the continuation shift ratio  ([H3-fast])   */
+  float video_fps;      /* [24] denominator of the continuation shift ratio            */
+} h3_rope_cfg;
+
+/* Modality-tagged rotary position encoding of Q and K, with the continuation time shift.
+ *
+ * [H3-vLLM] sec. 3 (tags choose the RoPE treatment; modality position spaces independent) and
+ * [H3-fast] "Crossing the time boundary" step 3 (t_global = t_local + s * 40/24, time only).
+ *
+ * For token i of request r with tag tau and local position (t, h, w) = pos[i]:
+ *   t_g = t + s_r * audio_hz / video_fps   (s_r = start_frames[r]; fp32, correctly rounded)
+ *   pairs (x[2j], x[2j+1]) are rotated by phi_j:
+ *     text / audio : phi_j = t_g * base^(-2j/D),                  j in [0, D/2)
+ *     video        : band t dims [0,d_t): t_g * base^(-2j/d_t); band h: h * base^(-2j/d_h);
+ *                    band w: w * base^(-2j/d_w)   (j counts pairs within the band)
+ *   x'[2j] = x[2j] cos phi - x[2j+1] sin phi;   x'[2j+1] = x[2j] sin phi + x[2j+1] cos phi
+ *
+ * q_in, q_out : device bf16 [C, H, D]; q_out may equal q_in (in place) but must not otherwise
+ *               overlap it.  Only rows [0, num_tokens) are read and written.
+ * k_in, k_out : same for K; both NULL to rotate Q only.
+ * pos         : device fp32 [num_tokens, 3] local (t, h, w); h, w ignored for text/audio.
+ * tag         : device uint8 [num_tokens]; values other than 1 (video) / 2 (audio) act as text.
+ * cu_requests : device int32 [num_requests + 1], request row offsets (0-based, non-decreasing,
+ *               last = num_tokens); NULL means one request covering every row.
+ * start_frames: device fp32 [num_requests], continuation start frame s_r; NULL means all 0.
+ * cfg         : host pointer, or NULL for all defaults.
+ * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG, H3_ERR_UNSUPPORTED, H3_ERR_MISALIGNED, H3_ERR_CUDA.
+ */
+H3_API h3_status h3_rope_apply(const void* q_in, void* q_out, const void* k_in, void* k_out,
+                        int32_t num_tokens, int32_t num_heads, int32_t head_dim,
+                        const float* pos, const uint8_t* tag,
+                        const int32_t* cu_requests, int32_t num_requests,
+                        const float* start_frames, const h3_rope_cfg* cfg, h3_stream_t stream);
+
+/* Bytes of device workspace h3_varlen_attn_fwd needs for these sizes (may be 0). */
+H3_API size_t h3_varlen_attn_workspace_size(int32_t num_segments, int32_t num_heads,
+                                     int32_t max_seqlen, int32_t head_dim);
+
+/* Block-diagonal (packed varlen) softmax attention forward, non-causal.
+ *
+ * [H3-vLLM] sec. 3: for segment g = [cu[g], cu[g+1]), head h and query row i in g,
+ *   S_ij = scale * <q_i, k_j> for j in g only;  P = softmax_j(S);  o_i = sum_j P_ij v_j;
+ *   lse_i = log sum_j exp(S_ij).  Keys outside g get weight exactly zero (they are never
+ *   multiplied in, so NaN/Inf there cannot leak).  [H3-vLLM] sec. 6: rows >= cu[S] are never
+ *   read as contributing keys/values and never written (trim = length only, no copy).
+ *
+ * q, k, v     : device bf16 [capacity, H, D].
+ * o           : device bf16 [capacity, H, D]; rows of every segment written, others untouched.
+ * lse         : device fp32 [H, capacity] (natural log) or NULL.
+ * cu_seqlens  : device int32 [num_segments + 1]; must start at 0, not decrease, end <= capacity.
+ *               Empty segments are allowed.
+ * max_seqlen  : host upper bound on the longest segment (sizes the launch).
+ * softmax_scale: <= 0 selects 1/sqrt(head_dim).
+ * workspace   : device scratch of h3_varlen_attn_workspace_size() bytes (16-byte aligned), or
+ *               NULL when that size is 0.  Contents need not be initialised.
+ * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG, H3_ERR_UNSUPPORTED, H3_ERR_MISALIGNED,
+ *         H3_ERR_WORKSPACE, H3_ERR_CUDA; device-side H3_ERR_BAD_CU_SEQLENS / H3_ERR_TIMEOUT.
+ */
+H3_API h3_status h3_varlen_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const int32_t* cu_seqlens, int32_t num_segments, int32_t max_seqlen,
+                             int32_t capacity, int32_t num_heads, int32_t head_dim,
+                             float softmax_scale, void* workspace, size_t workspace_bytes,
+                             h3_stream_t stream);
+
+/* Number of windows of the partition (host only; no device work).
+ * [H3-fast] "window attention across GPUs": along each axis of length L with window w and
+ * shift s there are ceil((L + s) / w) windows (edge windows cropped).  Returns -1 on bad input
+ * (non-positive grid or window, shift < 0 or >= window). */
+H3_API int32_t h3_window_count(const int32_t grid[3], const int32_t win[3], const int32_t shift[3]);
+
+/* Shifted 3D window partition + gather of rows into per-window segments.
+ *
+ * [H3-fast] "window attention across GPUs": the (T, H, W) token grid (row-major order) is cut
+ * into windows; token (t, h, w) belongs to axis windows floor((x + s) / w); windows are
+ * numbered lexicographically (i_t, i_h, i_w); the packed order lists windows by number and,
+ * inside a window, tokens by their original row-major index.
+ *
+ * grid, win, shift: host int32[3] each (T, H, W order).
+ * perm       : device int32 [N] out, perm[j] = original row of packed row j (N = T*H*W).
+ * cu_seqlens : device int32 [nwin + 1] out (nwin = h3_window_count()).
+ * src, dst   : host arrays of num_tensors device pointers; dst[i] row j = src[i] row perm[j].
+ *              Each tensor is [N, row_bytes]; dst must not overlap src.  num_tensors may be 0
+ *              (indexing only), at most 8.
+ * row_bytes  : bytes per row (e.g. H * D * 2), a positive multiple of 16.
+ * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG, H3_ERR_MISALIGNED, H3_ERR_CUDA.
+ */
+H3_API h3_status h3_window_pack(const int32_t grid[3], const int32_t win[3], const int32_t shift[3],
+                         int32_t* perm, int32_t* cu_seqlens,
+                         const void* const* src, void* const* dst, int32_t num_tensors,
+                         int32_t row_bytes, h3_stream_t stream);
+
+/* Restore original token order: dst row perm[j] = src row j, for j in [0, num_tokens).
+ * [H3-fast] "window attention across GPUs" (token order restored after attention).
+ * perm is device int32 [num_tokens] (a permutation of [0, num_tokens); an entry out of range is
+ * skipped and recorded as H3_ERR_BAD_PERM).  src, dst device [num_tokens, row_bytes], disjoint.
+ * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG, H3_ERR_MISALIGNED, H3_ERR_CUDA. */
+H3_API h3_status h3_window_unpack(const int32_t* perm, int32_t num_tokens, const void* src, void* dst,
+                           int32_t row_bytes, h3_stream_t stream);
+
+/* Synchronises `stream`, returns the first device-side error recorded on the current device
+ * since the last call (H3_OK if none) and clears it. */
+H3_API h3_status h3_get_device_error(h3_stream_t stream);
+
+/* Static description of a status code. */
+H3_API const char* h3_status_string(h3_status status);
+
+/* Library ABI version (major * 100 + minor). */
+H3_API int32_t h3_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H3ATTN_H_ */

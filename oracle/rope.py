@@ -118,16 +118,27 @@ def request_time_offsets(n_tokens: int, cu_requests: Optional[Sequence[int]],
 
 
 def rope_apply(x, pos, tag, cu_requests=None, start_frames=None, cfg: Optional[RopeConfig] = None,
-               num_tokens: Optional[int] = None) -> np.ndarray:
+               num_tokens: Optional[int] = None, rows: Optional[np.ndarray] = None) -> np.ndarray:
     """Tagged RoPE of x [C, H, D] for the first num_tokens rows (rest returned as NaN).
 
     cu_requests [R+1] / start_frames [R]: continuation requests packed in the sequence; each
     token's time coordinate is shifted by its request's s * 40/24 before the rotation.
+    rows: optional subset of row indices (< num_tokens) to evaluate; the result then has
+    len(rows) rows, in that order.
     """
+    if rows is not None:
+        rows = np.asarray(rows, dtype=np.int64)
     if hasattr(x, "detach"):
-        x = x.detach().float().numpy()
+        x = (x[rows] if rows is not None else x).detach().float().numpy()
+    elif rows is not None:
+        x = np.asarray(x)[rows]
     x = np.asarray(x, dtype=np.float64)
     C, H, D = x.shape
+    if rows is not None:
+        n_all = int(np.max(rows)) + 1 if rows.size else 0
+        off = request_time_offsets(n_all, cu_requests, start_frames, cfg)[rows]
+        phi = rope_angles(np.asarray(pos)[rows], np.asarray(tag)[rows], D, cfg, off)
+        return rotate_pairs(x, phi)
     n = C if num_tokens is None else int(num_tokens)
     off = request_time_offsets(n, cu_requests, start_frames, cfg)
     phi = rope_angles(np.asarray(pos)[:n], np.asarray(tag)[:n], D, cfg, off)

@@ -1,0 +1,288 @@
+"""GB300-native packed varlen attention with modality-tagged 3D RoPE.
+
+Thin Python binding over the C ABI of ``libh3attn.so`` (declared in include/h3attn.h).  It only
+marshals arguments -- checks dtypes and shapes, takes device pointers and the current CUDA
+stream from PyTorch tensors -- and every step of the computation runs in the library's CUDA
+kernels.  There is no CPU or PyTorch fallback: if the library is missing, every call raises.
+
+Calls:
+  rope_apply        modality-tagged RoPE of Q and K with the continuation time shift
+  varlen_attn_fwd   block-diagonal softmax attention over cu_seqlens segments
+  window_count / window_pack / window_unpack   shifted 3D window partition and row gather/scatter
+  get_device_error  read (and clear) the device-side error word
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+__all__ = ["H3Error", "RopeConfig", "lib_path", "load_library", "rope_apply", "varlen_attn_fwd",
+           "varlen_attn_workspace_size", "window_count", "window_pack", "window_unpack",
+           "get_device_error", "TAG_TEXT", "TAG_VIDEO", "TAG_AUDIO"]
+
+TAG_TEXT, TAG_VIDEO, TAG_AUDIO = 0, 1, 2
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libh3attn.so"
+_lib = None
+
+_STATUS = {0: "H3_OK", 1: "H3_ERR_NULL", 2: "H3_ERR_INVALID_ARG", 3: "H3_ERR_BAD_CU_SEQLENS",
+           4: "H3_ERR_UNSUPPORTED", 5: "H3_ERR_WORKSPACE", 6: "H3_ERR_CUDA", 7: "H3_ERR_TIMEOUT",
+           8: "H3_ERR_MISALIGNED", 9: "H3_ERR_BAD_PERM"}
+
+
+class H3Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        self.name = _STATUS.get(self.status, f"status {status}")
+        msg = load_library().h3_status_string(self.status).decode()
+        super().__init__(f"{where}: {self.name}: {msg}")
+
+
+class RopeConfig(ctypes.Structure):
+    """Mirror of h3_rope_cfg; zero fields select the defaults (base 10000, D/2:D/4:D/4, 40/24)."""
+    _fields_ = [("base_text", ctypes.c_float), ("base_video", ctypes.c_float),
+                ("base_audio", ctypes.c_float), ("video_dims_t", ctypes.c_int32),
+                ("video_dims_h", ctypes.c_int32), ("video_dims_w", ctypes.c_int32),
+                ("audio_hz", ctypes.c_float), ("video_fps", ctypes.c_float)]
+
+
+def lib_path() -> str:
+    return os.path.join(_PKG_DIR, _LIB_NAME)
+
+
+def load_library():
+    """Load libh3attn.so (built in-tree by __graft_entry__.build()); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run `python -c 'import __graft_entry__ as g; "
+                           "g.build()'` first (this package has no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    P, I32, U64, F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+    I32P = ctypes.POINTER(ctypes.c_int32)
+    sigs = {
+        "h3_rope_apply": (I32, [P, P, P, P, I32, I32, I32, P, P, P, I32, P,
+                                ctypes.POINTER(RopeConfig), P]),
+        "h3_varlen_attn_workspace_size": (U64, [I32, I32, I32, I32]),
+        "h3_varlen_attn_fwd": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, F32, P, U64, P]),
+        "h3_window_count": (I32, [I32P, I32P, I32P]),
+        "h3_window_pack": (I32, [I32P, I32P, I32P, P, P, ctypes.POINTER(P), ctypes.POINTER(P),
+                                 I32, I32, P]),
+        "h3_window_unpack": (I32, [P, I32, P, P, I32, P]),
+        "h3_get_device_error": (I32, [P]),
+        "h3_status_string": (ctypes.c_char_p, [I32]),
+        "h3_version": (I32, []),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise H3Error(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _require(t: torch.Tensor, name: str, dtype, device: torch.device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _i3(v: Sequence[int]):
+    a = (ctypes.c_int32 * 3)(*[int(x) for x in v])
+    return a
+
+
+def rope_apply(q: torch.Tensor, k: Optional[torch.Tensor], pos: torch.Tensor, tag: torch.Tensor,
+               cu_requests: Optional[torch.Tensor] = None, start_frames: Optional[torch.Tensor] = None,
+               num_tokens: Optional[int] = None, q_out: Optional[torch.Tensor] = None,
+               k_out: Optional[torch.Tensor] = None, cfg: Optional[RopeConfig] = None):
+    """Tagged RoPE of q (and k) [C, H, D] bf16; in place unless q_out / k_out are given.
+
+    pos fp32 [>=N, 3] (t, h, w); tag uint8 [>=N]; cu_requests int32 [R+1] and start_frames fp32
+    [R] (continuation start frames s_r) are optional.  Returns (q_out, k_out).
+    """
+    dev = q.device
+    _require(q, "q", torch.bfloat16, dev)
+    if q.dim() != 3:
+        raise ValueError("q must be [C, H, D]")
+    C, H, D = q.shape
+    n = C if num_tokens is None else int(num_tokens)
+    if n > C:
+        raise ValueError("num_tokens exceeds the capacity of q")
+    q_out = q if q_out is None else q_out
+    _require(q_out, "q_out", torch.bfloat16, dev)
+    if k is not None:
+        _require(k, "k", torch.bfloat16, dev)
+        k_out = k if k_out is None else k_out
+        _require(k_out, "k_out", torch.bfloat16, dev)
+        if k.shape != q.shape or k_out.shape != q.shape:
+            raise ValueError("k must have q's shape")
+    else:
+        k_out = None
+    if q_out.shape != q.shape:
+        raise ValueError("q_out must have q's shape")
+    _require(pos, "pos", torch.float32, dev)
+    _require(tag, "tag", torch.uint8, dev)
+    if pos.shape[0] < n or tag.shape[0] < n:
+        raise ValueError("pos / tag must cover num_tokens rows")
+    nreq = 0
+    if cu_requests is not None:
+        _require(cu_requests, "cu_requests", torch.int32, dev)
+        nreq = cu_requests.numel() - 1
+    if start_frames is not None:
+        _require(start_frames, "start_frames", torch.float32, dev)
+        if cu_requests is not None and start_frames.numel() < nreq:
+            raise ValueError("start_frames must have one entry per request")
+    lib = load_library()
+    with torch.cuda.device(dev):
+        st = lib.h3_rope_apply(_ptr(q), _ptr(q_out), _ptr(k), _ptr(k_out), n, H, D, _ptr(pos),
+                               _ptr(tag), _ptr(cu_requests), nreq, _ptr(start_frames),
+                               ctypes.byref(cfg) if cfg is not None else None, _stream(dev))
+    _check(st, "h3_rope_apply")
+    return q_out, k_out
+
+
+def varlen_attn_workspace_size(num_segments: int, num_heads: int, max_seqlen: int, head_dim: int) -> int:
+    return int(load_library().h3_varlen_attn_workspace_size(num_segments, num_heads, max_seqlen, head_dim))
+
+
+def varlen_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+                    max_seqlen: int, out: Optional[torch.Tensor] = None, return_lse: bool = False,
+                    lse: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None,
+                    workspace: Optional[torch.Tensor] = None):
+    """Block-diagonal attention over the segments of cu_seqlens (int32 [S+1], device).
+
+    q, k, v: bf16 [C, H, D] with C >= cu_seqlens[-1].  Rows of `out` outside every segment are
+    left untouched.  Returns out (and lse fp32 [H, C] when requested).
+    """
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name, torch.bfloat16, dev)
+    if q.dim() != 3 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all be [C, H, D]")
+    C, H, D = q.shape
+    _require(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    S = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out, "out", torch.bfloat16, dev)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if return_lse and lse is None:
+        lse = torch.empty((H, C), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _require(lse, "lse", torch.float32, dev)
+        if tuple(lse.shape) != (H, C):
+            raise ValueError("lse must be [H, C]")
+    lib = load_library()
+    ws_need = int(lib.h3_varlen_attn_workspace_size(S, H, int(max_seqlen), D))
+    if ws_need > 0 and workspace is None:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    with torch.cuda.device(dev):
+        st = lib.h3_varlen_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                    _ptr(cu_seqlens), S, int(max_seqlen), C, H, D, scale,
+                                    _ptr(workspace), ws_bytes, _stream(dev))
+    _check(st, "h3_varlen_attn_fwd")
+    return (out, lse) if (return_lse or lse is not None) else out
+
+
+def window_count(grid: Sequence[int], win: Sequence[int], shift: Sequence[int]) -> int:
+    n = load_library().h3_window_count(_i3(grid), _i3(win), _i3(shift))
+    if n < 0:
+        raise ValueError("invalid window geometry")
+    return int(n)
+
+
+def window_pack(grid: Sequence[int], win: Sequence[int], shift: Sequence[int],
+                tensors: Sequence[torch.Tensor] = (), device: Optional[torch.device] = None,
+                perm: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None,
+                outs: Optional[Sequence[torch.Tensor]] = None):
+    """Partition the (T, H, W) grid into (shifted) windows and gather each tensor's rows.
+
+    tensors: [N, ...] contiguous, same device, N = T*H*W.  Returns (perm, cu_seqlens, packed).
+    """
+    nwin = window_count(grid, win, shift)
+    n = int(grid[0]) * int(grid[1]) * int(grid[2])
+    dev = tensors[0].device if tensors else (device or torch.device("cuda"))
+    if perm is None:
+        perm = torch.empty(n, dtype=torch.int32, device=dev)
+    if cu_seqlens is None:
+        cu_seqlens = torch.empty(nwin + 1, dtype=torch.int32, device=dev)
+    _require(perm, "perm", torch.int32, dev)
+    _require(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    if perm.numel() < n or cu_seqlens.numel() < nwin + 1:
+        raise ValueError("perm / cu_seqlens too small")
+    outs = list(outs) if outs is not None else [torch.empty_like(t) for t in tensors]
+    row_bytes = 0
+    for i, (t, o) in enumerate(zip(tensors, outs)):
+        if not t.is_contiguous() or not o.is_contiguous() or t.device != dev or o.device != dev:
+            raise ValueError("window_pack tensors must be contiguous on one device")
+        if t.shape[0] != n or o.shape != t.shape or o.dtype != t.dtype:
+            raise ValueError("each tensor must have T*H*W rows and a matching output")
+        rb = t[0].numel() * t.element_size()
+        if i and rb != row_bytes:
+            raise ValueError("all tensors must share one row size")
+        row_bytes = rb
+    k = len(tensors)
+    src = (ctypes.c_void_p * max(k, 1))(*[t.data_ptr() for t in tensors])
+    dst = (ctypes.c_void_p * max(k, 1))(*[o.data_ptr() for o in outs])
+    lib = load_library()
+    with torch.cuda.device(dev):
+        st = lib.h3_window_pack(_i3(grid), _i3(win), _i3(shift), _ptr(perm), _ptr(cu_seqlens),
+                                src, dst, k, row_bytes, _stream(dev))
+    _check(st, "h3_window_pack")
+    return perm, cu_seqlens, outs
+
+
+def window_unpack(perm: torch.Tensor, src: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Restore original order: out[perm[j]] = src[j]."""
+    dev = src.device
+    _require(perm, "perm", torch.int32, dev)
+    if not src.is_contiguous():
+        raise ValueError("src must be contiguous")
+    n = src.shape[0]
+    if perm.numel() < n:
+        raise ValueError("perm too small")
+    out = torch.empty_like(src) if out is None else out
+    if out.shape != src.shape or out.dtype != src.dtype or not out.is_contiguous():
+        raise ValueError("out must match src")
+    row_bytes = src[0].numel() * src.element_size()
+    lib = load_library()
+    with torch.cuda.device(dev):
+        st = lib.h3_window_unpack(_ptr(perm), n, _ptr(src), _ptr(out), row_bytes, _stream(dev))
+    _check(st, "h3_window_unpack")
+    return out
+
+
+def get_device_error(device: Optional[torch.device] = None) -> int:
+    """Synchronise the current stream; return and clear the device error word (0 = none)."""
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    lib = load_library()
+    with torch.cuda.device(dev):
+        return int(lib.h3_get_device_error(_stream(dev)))

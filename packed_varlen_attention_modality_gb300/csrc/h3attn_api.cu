@@ -1,0 +1,280 @@
+// C ABI of libh3attn: argument validation, tensor-map construction, kernel launch.
+//
+// Nothing here allocates device memory.  The one piece of library-owned device state is the
+// error word below (a static __device__ variable, 4 bytes per device), where kernels record the
+// first device-side problem they meet (bad cu_seqlens, bad permutation entry, a timed-out wait).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "h3attn.h"
+#include "h3_internal.h"
+
+namespace {
+
+__device__ unsigned int g_device_error;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+unsigned int* g_err_ptr[kMaxDevices] = {};
+
+// Device address of g_device_error on the current device (looked up once per device).
+unsigned int* device_error_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D view {D, H, rows} of a bf16 [rows, H, D] tensor; box {64, 1, 128}, 128-byte swizzle.
+bool make_qkv_map(CUtensorMap* m, const void* base, int rows, int heads, int head_dim) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                 static_cast<cuuint64_t>(heads) * head_dim * 2};
+  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool device_is_sm103() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return false;
+  return major == 10 && minor == 3;
+}
+
+h3_status from_cuda(cudaError_t e) { return e == cudaSuccess ? H3_OK : H3_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t h3_version(void) { return 100; }
+
+const char* h3_status_string(h3_status s) {
+  switch (s) {
+    case H3_OK: return "ok";
+    case H3_ERR_NULL: return "a required pointer is NULL";
+    case H3_ERR_INVALID_ARG: return "a size or scalar argument is out of range";
+    case H3_ERR_BAD_CU_SEQLENS:
+      return "cu_seqlens is not 0-based and non-decreasing within capacity, or a segment exceeds "
+             "max_seqlen";
+    case H3_ERR_UNSUPPORTED: return "unsupported head_dim or device (needs sm_103a, D in {64,128})";
+    case H3_ERR_WORKSPACE: return "workspace missing or too small";
+    case H3_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    case H3_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    case H3_ERR_MISALIGNED: return "a device pointer or row size is not 16-byte aligned";
+    case H3_ERR_BAD_PERM: return "a permutation entry is out of range";
+  }
+  return "unknown status";
+}
+
+h3_status h3_get_device_error(h3_stream_t stream) {
+  unsigned int* p = device_error_ptr();
+  if (p == nullptr) return H3_ERR_CUDA;
+  unsigned int host = 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&host, p, sizeof(host), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return H3_ERR_CUDA;
+  if (cudaMemsetAsync(p, 0, sizeof(unsigned int), st) != cudaSuccess) return H3_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return H3_ERR_CUDA;
+  return static_cast<h3_status>(host);
+}
+
+h3_status h3_rope_apply(const void* q_in, void* q_out, const void* k_in, void* k_out,
+                        int32_t num_tokens, int32_t num_heads, int32_t head_dim,
+                        const float* pos, const uint8_t* tag, const int32_t* cu_requests,
+                        int32_t num_requests, const float* start_frames,
+                        const h3_rope_cfg* cfg, h3_stream_t stream) {
+  if (q_in == nullptr || q_out == nullptr || pos == nullptr || tag == nullptr) return H3_ERR_NULL;
+  if ((k_in == nullptr) != (k_out == nullptr)) return H3_ERR_NULL;
+  if (num_tokens < 0 || num_heads <= 0) return H3_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return H3_ERR_UNSUPPORTED;
+  if (cu_requests != nullptr && num_requests <= 0) return H3_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_tokens) * num_heads * head_dim / 8 > INT32_MAX)
+    return H3_ERR_INVALID_ARG;
+  if (!aligned16(q_in) || !aligned16(q_out) || (k_in && (!aligned16(k_in) || !aligned16(k_out))))
+    return H3_ERR_MISALIGNED;
+
+  h3_rope_cfg c{};
+  if (cfg != nullptr) c = *cfg;
+  const double base_t = c.base_text > 0 ? c.base_text : 10000.0;
+  const double base_v = c.base_video > 0 ? c.base_video : 10000.0;
+  const double base_a = c.base_audio > 0 ? c.base_audio : 10000.0;
+  int dt = c.video_dims_t, dh = c.video_dims_h, dw = c.video_dims_w;
+  if (dt == 0 && dh == 0 && dw == 0) {
+    dt = head_dim / 2;
+    dh = head_dim / 4;
+    dw = head_dim / 4;
+  }
+  if (dt < 0 || dh < 0 || dw < 0 || dt + dh + dw != head_dim || (dt | dh | dw) & 1)
+    return H3_ERR_INVALID_ARG;
+
+  // Frequency ladders, fp64 on the host, rounded once to fp32: theta_j = base^(-2j/d).
+  h3::RopeTables tab{};
+  const int P = head_dim / 2;
+  for (int j = 0; j < P; ++j) {
+    tab.inv_text[j] = static_cast<float>(std::pow(base_t, -2.0 * j / head_dim));
+    tab.inv_audio[j] = static_cast<float>(std::pow(base_a, -2.0 * j / head_dim));
+    int axis, jl, d;
+    if (j < dt / 2) { axis = 0; jl = j; d = dt; }
+    else if (j < (dt + dh) / 2) { axis = 1; jl = j - dt / 2; d = dh; }
+    else { axis = 2; jl = j - (dt + dh) / 2; d = dw; }
+    tab.video_axis[j] = static_cast<uint8_t>(axis);
+    tab.inv_video[j] = static_cast<float>(std::pow(base_v, -2.0 * jl / d));
+  }
+  tab.audio_hz = c.audio_hz > 0 ? c.audio_hz : 40.f;
+  tab.video_fps = c.video_fps > 0 ? c.video_fps : 24.f;
+
+  const int nreq = cu_requests ? num_requests : 1;
+  return from_cuda(h3::launch_rope(q_in, q_out, k_in, k_out, num_tokens, num_heads, head_dim, pos,
+                                   tag, cu_requests, nreq, start_frames, tab,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t h3_varlen_attn_workspace_size(int32_t num_segments, int32_t num_heads, int32_t max_seqlen,
+                                     int32_t head_dim) {
+  (void)num_segments;
+  (void)num_heads;
+  (void)max_seqlen;
+  (void)head_dim;
+  return 0;
+}
+
+h3_status h3_varlen_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const int32_t* cu_seqlens, int32_t num_segments, int32_t max_seqlen,
+                             int32_t capacity, int32_t num_heads, int32_t head_dim,
+                             float softmax_scale, void* workspace, size_t workspace_bytes,
+                             h3_stream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || cu_seqlens == nullptr)
+    return H3_ERR_NULL;
+  if (num_segments < 0 || num_segments > 65535 || max_seqlen < 0 || capacity < 0 ||
+      num_heads <= 0 || num_heads > 65535)
+    return H3_ERR_INVALID_ARG;
+  if (max_seqlen > capacity) return H3_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return H3_ERR_UNSUPPORTED;
+  if (!(softmax_scale <= 0.f || std::isfinite(softmax_scale))) return H3_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return H3_ERR_MISALIGNED;
+  const size_t need = h3_varlen_attn_workspace_size(num_segments, num_heads, max_seqlen, head_dim);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return H3_ERR_WORKSPACE;
+  if (num_segments == 0 || max_seqlen == 0 || capacity == 0) return H3_OK;
+  if (!device_is_sm103()) return H3_ERR_UNSUPPORTED;
+
+  h3::AttnArgs a{};
+  if (!make_qkv_map(&a.tmap_q, q, capacity, num_heads, head_dim) ||
+      !make_qkv_map(&a.tmap_k, k, capacity, num_heads, head_dim) ||
+      !make_qkv_map(&a.tmap_v, v, capacity, num_heads, head_dim))
+    return H3_ERR_CUDA;
+  a.o = o;
+  a.lse = lse;
+  a.cu_seqlens = cu_seqlens;
+  a.num_segments = num_segments;
+  a.max_seqlen = max_seqlen;
+  a.capacity = capacity;
+  a.num_heads = num_heads;
+  a.head_dim = head_dim;
+  a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(head_dim));
+  a.err = device_error_ptr();
+  if (a.err == nullptr) return H3_ERR_CUDA;
+  return from_cuda(h3::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t h3_window_count(const int32_t grid[3], const int32_t win[3], const int32_t shift[3]) {
+  if (grid == nullptr || win == nullptr || shift == nullptr) return -1;
+  int64_t n = 1;
+  for (int a = 0; a < 3; ++a) {
+    if (grid[a] <= 0 || win[a] <= 0 || shift[a] < 0 || shift[a] >= win[a]) return -1;
+    n *= (static_cast<int64_t>(grid[a]) + shift[a] + win[a] - 1) / win[a];
+  }
+  return n > INT32_MAX ? -1 : static_cast<int32_t>(n);
+}
+
+h3_status h3_window_pack(const int32_t grid[3], const int32_t win[3], const int32_t shift[3],
+                         int32_t* perm, int32_t* cu_seqlens, const void* const* src,
+                         void* const* dst, int32_t num_tensors, int32_t row_bytes,
+                         h3_stream_t stream) {
+  if (grid == nullptr || win == nullptr || shift == nullptr || perm == nullptr ||
+      cu_seqlens == nullptr)
+    return H3_ERR_NULL;
+  if (num_tensors < 0 || num_tensors > h3::kMaxPackTensors) return H3_ERR_INVALID_ARG;
+  if (num_tensors > 0 && (src == nullptr || dst == nullptr)) return H3_ERR_NULL;
+  const int32_t nwin = h3_window_count(grid, win, shift);
+  if (nwin < 0) return H3_ERR_INVALID_ARG;
+  const int64_t n = static_cast<int64_t>(grid[0]) * grid[1] * grid[2];
+  if (n > INT32_MAX / 2) return H3_ERR_INVALID_ARG;
+  h3::PackPtrs ptrs{};
+  if (num_tensors > 0) {
+    if (row_bytes <= 0 || (row_bytes & 15)) return H3_ERR_MISALIGNED;
+    for (int i = 0; i < num_tensors; ++i) {
+      if (src[i] == nullptr || dst[i] == nullptr) return H3_ERR_NULL;
+      if (!aligned16(src[i]) || !aligned16(dst[i])) return H3_ERR_MISALIGNED;
+      ptrs.src[i] = src[i];
+      ptrs.dst[i] = dst[i];
+    }
+  }
+  h3::WindowGeom g{};
+  for (int a = 0; a < 3; ++a) {
+    g.L[a] = grid[a];
+    g.w[a] = win[a];
+    g.s[a] = shift[a];
+    g.nwin[a] = (grid[a] + shift[a] + win[a] - 1) / win[a];
+  }
+  return from_cuda(h3::launch_window_pack(g, perm, cu_seqlens, ptrs, num_tensors, row_bytes,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+h3_status h3_window_unpack(const int32_t* perm, int32_t num_tokens, const void* src, void* dst,
+                           int32_t row_bytes, h3_stream_t stream) {
+  if (perm == nullptr || src == nullptr || dst == nullptr) return H3_ERR_NULL;
+  if (num_tokens < 0) return H3_ERR_INVALID_ARG;
+  if (row_bytes <= 0 || (row_bytes & 15)) return H3_ERR_MISALIGNED;
+  if (!aligned16(src) || !aligned16(dst)) return H3_ERR_MISALIGNED;
+  unsigned int* err = device_error_ptr();
+  if (err == nullptr) return H3_ERR_CUDA;
+  return from_cuda(h3::launch_window_unpack(perm, num_tokens, src, dst, row_bytes, err,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,130 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every symbol the header
+declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "h3attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import packed_varlen_attention_modality_gb300 as h3
+
+    return h3.load_library()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"H3_API\s+[\w\s\*]+?\b(h3_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary_calls():
+    names = _declared()
+    for must in ["h3_rope_apply", "h3_varlen_attn_fwd", "h3_varlen_attn_workspace_size",
+                 "h3_window_count", "h3_window_pack", "h3_window_unpack", "h3_get_device_error",
+                 "h3_status_string", "h3_version"]:
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_library_exports_nothing_else():
+    import subprocess
+    import packed_varlen_attention_modality_gb300 as h3
+
+    out = subprocess.run(["nm", "-D", "--defined-only", h3.lib_path()], capture_output=True, text=True).stdout
+    exported = sorted({l.split()[-1] for l in out.splitlines() if " T " in l})
+    assert exported == _declared()
+
+
+def test_version_and_status_strings(lib):
+    assert lib.h3_version() == 100
+    for s in range(10):
+        assert len(lib.h3_status_string(s)) >= 2
+    assert lib.h3_status_string(99) == b"unknown status"
+
+
+def _i3(v):
+    return (ctypes.c_int32 * 3)(*v)
+
+
+@pytest.mark.parametrize("grid,win,shift", [((32, 48, 84), (4, 8, 8), (0, 0, 0)),
+                                            ((32, 48, 84), (4, 8, 8), (2, 4, 4)),
+                                            ((5, 6, 7), (2, 4, 4), (1, 2, 2)),
+                                            ((1, 1, 1), (4, 8, 8), (3, 7, 7))])
+def test_window_count_matches_oracle(lib, grid, win, shift):
+    assert lib.h3_window_count(_i3(grid), _i3(win), _i3(shift)) == oracle.window_count(grid, win, shift)
+
+
+@pytest.mark.parametrize("grid,win,shift", [((0, 4, 4), (2, 2, 2), (0, 0, 0)), ((4, 4, 4), (2, 0, 2), (0, 0, 0)),
+                                            ((4, 4, 4), (2, 2, 2), (2, 0, 0)), ((4, 4, 4), (2, 2, 2), (-1, 0, 0))])
+def test_window_count_rejects_bad_geometry(lib, grid, win, shift):
+    assert lib.h3_window_count(_i3(grid), _i3(win), _i3(shift)) == -1
+
+
+FAKE = 0x1000  # never dereferenced: every call below is rejected by host-side validation
+
+
+def test_attn_rejects_bad_arguments_on_the_host(lib):
+    f = lib.h3_varlen_attn_fwd
+    P = ctypes.c_void_p
+    ok = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, cu=FAKE, S=3, maxs=128, C=256, H=2, D=128)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(P(a["q"]), P(a["k"]), P(a["v"]), P(a["o"]), P(a["lse"]) if a["lse"] else None,
+                 P(a["cu"]) if a["cu"] else None, a["S"], a["maxs"], a["C"], a["H"], a["D"], 0.0, None, 0, None)
+
+    assert call(q=0) == 1 and call(cu=0) == 1 and call(o=0) == 1          # H3_ERR_NULL
+    assert call(S=-1) == 2 and call(H=0) == 2 and call(maxs=512) == 2      # max_seqlen > capacity
+    assert call(D=96) == 4                                                # H3_ERR_UNSUPPORTED
+    assert call(q=FAKE + 8) == 8 and call(lse=FAKE + 2) == 8              # H3_ERR_MISALIGNED
+    assert call(S=0) == 0 and call(maxs=0) == 0                           # nothing to do
+
+
+def test_rope_rejects_bad_arguments_on_the_host(lib):
+    f = lib.h3_rope_apply
+    P = ctypes.c_void_p
+
+    def call(q=FAKE, qo=FAKE, k=FAKE, ko=FAKE, n=10, H=2, D=64, pos=FAKE, tag=FAKE, cu=None, R=0, cfg=None):
+        return f(P(q) if q else None, P(qo) if qo else None, P(k) if k else None, P(ko) if ko else None,
+                 n, H, D, P(pos) if pos else None, P(tag) if tag else None, P(cu) if cu else None, R, None,
+                 cfg, None)
+
+    assert call(q=0) == 1 and call(pos=0) == 1 and call(ko=0) == 1
+    assert call(n=-1) == 2 and call(H=0) == 2 and call(cu=FAKE, R=0) == 2
+    assert call(D=80) == 4
+    assert call(q=FAKE + 4) == 8
+    import packed_varlen_attention_modality_gb300 as h3
+
+    bad = h3.RopeConfig(video_dims_t=30, video_dims_h=16, video_dims_w=16)  # sums to 62 != 64
+    assert call(cfg=ctypes.byref(bad)) == 2
+    odd = h3.RopeConfig(video_dims_t=31, video_dims_h=17, video_dims_w=16)  # odd band width
+    assert call(cfg=ctypes.byref(odd)) == 2
+
+
+def test_window_calls_reject_bad_arguments_on_the_host(lib):
+    P = ctypes.c_void_p
+    src = (P * 1)(FAKE)
+    dst = (P * 1)(FAKE)
+    g, w, s = _i3((4, 8, 8)), _i3((2, 4, 4)), _i3((1, 2, 2))
+    assert lib.h3_window_pack(g, w, s, None, P(FAKE), src, dst, 1, 256, None) == 1
+    assert lib.h3_window_pack(g, w, s, P(FAKE), P(FAKE), src, dst, 9, 256, None) == 2
+    assert lib.h3_window_pack(g, w, s, P(FAKE), P(FAKE), src, dst, 1, 200, None) == 8
+    assert lib.h3_window_pack(g, w, _i3((2, 2, 2)), P(FAKE), P(FAKE), src, dst, 1, 256, None) == 2
+    assert lib.h3_window_unpack(P(FAKE), 16, P(FAKE + 8), P(FAKE), 256, None) == 8
+    assert lib.h3_window_unpack(None, 16, P(FAKE), P(FAKE), 256, None) == 1
+    assert lib.h3_window_unpack(P(FAKE), -2, P(FAKE), P(FAKE), 256, None) == 2

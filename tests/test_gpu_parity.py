@@ -1,0 +1,318 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU fp64 oracle.
+
+Tolerances (bf16 storage, fp32 math):
+  * bf16 outputs (RoPE, attention): max |err| <= 2e-2 and mean |err| <= 2e-3 against fp64;
+  * LSE: |err| <= 1e-4 * max(|lse|, 1)  (relative, with a floor of 1 for near-zero values);
+  * integer outputs (perm, cu_seqlens) and pure copies (window gather / restore): bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS, LSE_REL = 2e-2, 2e-3, 1e-4
+
+
+@pytest.fixture(scope="module")
+def h3():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import packed_varlen_attention_modality_gb300 as h3
+
+    h3.load_library()
+    return h3
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    d = torch.device("cuda", 0)
+    torch.cuda.set_device(d)
+    return d
+
+
+def _close(got, ref, what, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, what
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    assert err.max() <= max_abs and err.mean() <= mean_abs, \
+        f"{what}: max {err.max():.3e} mean {err.mean():.3e}"
+    return err.max(), err.mean()
+
+
+def _lse_close(got, ref, what):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rel = np.abs(got - ref) / np.maximum(np.abs(ref), 1.0)
+    assert rel.max() <= LSE_REL, f"{what}: lse rel {rel.max():.3e}"
+
+
+def _to(dev, wl):
+    return dict(q=wl.q.to(dev), k=wl.k.to(dev), v=wl.v.to(dev), pos=torch.from_numpy(wl.pos).to(dev),
+                tag=torch.from_numpy(wl.tag).to(dev), cu=torch.from_numpy(wl.cu_seqlens).to(dev),
+                cu_req=torch.from_numpy(wl.cu_requests).to(dev),
+                frames=torch.from_numpy(wl.start_frames).to(dev))
+
+
+def _sample_rows(cu, seed, edge=128, frac=256):
+    """Every row of short segments, the first/last `edge` rows of each segment, 1/frac of the rest."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for g in range(len(cu) - 1):
+        a, b = int(cu[g]), int(cu[g + 1])
+        if b - a <= 3 * edge:
+            rows.append(np.arange(a, b))
+            continue
+        rows += [np.arange(a, a + edge), np.arange(b - edge, b)]
+        mid = np.arange(a + edge, b - edge)
+        rows.append(rng.choice(mid, size=max(1, mid.size // frac), replace=False))
+    return np.unique(np.concatenate(rows))
+
+
+def _run_rope(h3, d, wl):
+    qr, kr = torch.empty_like(d["q"]), torch.empty_like(d["k"])
+    h3.rope_apply(d["q"], d["k"], d["pos"], d["tag"], d["cu_req"], d["frames"], num_tokens=wl.num_tokens,
+                  q_out=qr, k_out=kr)
+    return qr, kr
+
+
+PACKED = {
+    "tiny_example": lambda: W.tiny_example(capacity=64),
+    "single_request_4k": lambda: W.single_request_4k(capacity=4160),
+    "continuation_batch": lambda: W.continuation_batch(),
+    "h3_full_request": lambda: W.h3_full_request(),
+}
+FULL_CHECK = {"tiny_example", "single_request_4k"}
+
+
+@pytest.fixture(scope="module", params=list(PACKED))
+def packed_case(request, h3, dev):
+    wl = PACKED[request.param]()
+    d = _to(dev, wl)
+    qr, kr = _run_rope(h3, d, wl)
+    o, lse = h3.varlen_attn_fwd(qr, kr, d["v"], d["cu"], wl.max_seqlen, return_lse=True)
+    torch.cuda.synchronize()
+    assert h3.get_device_error(dev) == 0
+    full = request.param in FULL_CHECK
+    rows = np.arange(wl.num_tokens) if full else _sample_rows(wl.cu_seqlens, seed=len(request.param))
+    res = dict(wl=wl, rows=rows, full=full, q_rot=qr.cpu(), k_rot=kr.cpu(), o=o.cpu(), lse=lse.cpu())
+    del d, qr, kr, o, lse
+    torch.cuda.empty_cache()
+    return request.param, res
+
+
+def test_rope_parity(packed_case):
+    name, r = packed_case
+    wl, rows = r["wl"], r["rows"]
+    for t_in, t_out in ((wl.q, r["q_rot"]), (wl.k, r["k_rot"])):
+        ref = oracle.rope_apply(t_in, wl.pos, wl.tag, wl.cu_requests, wl.start_frames, rows=rows)
+        _close(t_out[rows].float().numpy(), ref, f"{name} rope")
+
+
+def test_attention_parity_on_gpu_rope_output(packed_case):
+    """Parity (i): attention alone, the oracle fed the GPU's own bf16 RoPE outputs."""
+    name, r = packed_case
+    wl, rows = r["wl"], r["rows"]
+    ref_o, ref_lse = oracle.varlen_attention(r["q_rot"], r["k_rot"], wl.v, wl.cu_seqlens, rows=rows)
+    _close(r["o"][rows].float().numpy(), ref_o[rows], f"{name} attention")
+    _lse_close(r["lse"][:, rows].numpy(), ref_lse[:, rows], f"{name} attention")
+
+
+def test_end_to_end_parity_from_raw_qk(packed_case):
+    """Parity (iii): the oracle does its own fp64 RoPE (with the time shift) from raw Q/K."""
+    name, r = packed_case
+    wl = r["wl"]
+    if not r["full"]:
+        # sampled rows need every key of their segment: restrict to the short segments + a slice
+        segs = [g for g in range(wl.num_segments) if wl.cu_seqlens[g + 1] - wl.cu_seqlens[g] <= 4096]
+        if not segs:
+            pytest.skip("no short segment to check end to end at this size")
+    else:
+        segs = list(range(wl.num_segments))
+    for g in segs:
+        a, b = int(wl.cu_seqlens[g]), int(wl.cu_seqlens[g + 1])
+        idx = np.arange(a, b)
+        qo = oracle.rope_apply(wl.q, wl.pos, wl.tag, wl.cu_requests, wl.start_frames, rows=idx)
+        ko = oracle.rope_apply(wl.k, wl.pos, wl.tag, wl.cu_requests, wl.start_frames, rows=idx)
+        vo = wl.v[a:b].double().numpy()
+        ref_o, ref_lse = oracle.varlen_attention(qo, ko, vo, [0, b - a])
+        _close(r["o"][a:b].float().numpy(), ref_o, f"{name} e2e seg {g}")
+        _lse_close(r["lse"][:, a:b].numpy(), ref_lse, f"{name} e2e seg {g}")
+
+
+def test_pad_rows_of_output_untouched(h3, dev):
+    wl = W.tiny_example(capacity=64)
+    d = _to(dev, wl)
+    o = torch.full_like(d["q"], 7.0)
+    h3.varlen_attn_fwd(d["q"], d["k"], d["v"], d["cu"], 20, out=o)
+    torch.cuda.synchronize()
+    assert torch.all(o[45:] == 7.0)
+    assert torch.all(torch.isfinite(o[:45].float()))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("lengths", [[1, 127, 128, 129, 0, 255, 256, 257, 2, 383],
+                                     [1000, 1, 1, 513], [0, 0, 77], [128 * 5]])
+def test_edge_lengths_against_oracle(h3, dev, D, lengths):
+    wl = W.random_packed(100 + sum(lengths) % 97, lengths, heads=3, head_dim=D,
+                         capacity=sum(lengths) + 61)
+    d = _to(dev, wl)
+    o = torch.full_like(d["q"], 3.0)
+    lse = torch.full((3, wl.capacity), 5.0, device=dev)
+    h3.varlen_attn_fwd(d["q"], d["k"], d["v"], d["cu"], max(1, wl.max_seqlen), out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert h3.get_device_error(dev) == 0
+    N = wl.num_tokens
+    ref_o, ref_lse = oracle.varlen_attention(wl.q, wl.k, wl.v, wl.cu_seqlens)
+    if N:
+        _close(o[:N].float().cpu().numpy(), ref_o[:N], f"lengths {lengths} D {D}")
+        _lse_close(lse[:, :N].cpu().numpy(), ref_lse[:, :N], f"lengths {lengths} D {D}")
+    assert torch.all(o[N:] == 3.0) and torch.all(lse[:, N:] == 5.0)
+
+
+def test_explicit_softmax_scale(h3, dev):
+    wl = W.random_packed(7, [300, 45], heads=2, head_dim=128)
+    d = _to(dev, wl)
+    o, lse = h3.varlen_attn_fwd(d["q"], d["k"], d["v"], d["cu"], 300, return_lse=True, softmax_scale=0.05)
+    ref_o, ref_lse = oracle.varlen_attention(wl.q, wl.k, wl.v, wl.cu_seqlens, scale=0.05)
+    _close(o.float().cpu().numpy(), ref_o, "scale 0.05")
+    _lse_close(lse.cpu().numpy(), ref_lse, "scale 0.05")
+
+
+@pytest.mark.parametrize("fill", [float("nan"), float("inf"), -float("inf"), 1e4])
+def test_out_of_segment_rows_cannot_leak(h3, dev, fill):
+    """The pages' pad failure: NaN/Inf outside a segment must not reach it -- bit-identical output."""
+    wl = W.random_packed(9, [200, 131, 256, 5], heads=2, head_dim=128, capacity=640)
+    d = _to(dev, wl)
+    base = h3.varlen_attn_fwd(d["q"], d["k"], d["v"], d["cu"], 256)
+    cu = wl.cu_seqlens
+    for g in range(len(cu) - 1):
+        a, b = int(cu[g]), int(cu[g + 1])
+        q, k, v = (t.clone() for t in (d["q"], d["k"], d["v"]))
+        for t in (q, k, v):
+            t[:a] = fill
+            t[b:] = fill
+        o = h3.varlen_attn_fwd(q, k, v, d["cu"], 256)
+        torch.cuda.synchronize()
+        assert torch.equal(o[a:b], base[a:b]), f"segment {g} changed under fill {fill}"
+
+
+def test_rope_in_place_equals_out_of_place(h3, dev):
+    wl = W.continuation_batch()
+    d = _to(dev, wl)
+    qr, kr = _run_rope(h3, d, wl)
+    q2, k2 = d["q"].clone(), d["k"].clone()
+    h3.rope_apply(q2, k2, d["pos"], d["tag"], d["cu_req"], d["frames"])
+    torch.cuda.synchronize()
+    assert torch.equal(q2, qr) and torch.equal(k2, kr)
+
+
+def test_uniform_time_shift_leaves_attention_unchanged(h3, dev):
+    """End-to-end invariant: shifting a whole request's time axis does not change its attention."""
+    wl = W.tiny_example()
+    d = _to(dev, wl)
+    outs = []
+    for s in (0.0, 238.0):
+        frames = torch.tensor([s], device=dev)
+        qr, kr = torch.empty_like(d["q"]), torch.empty_like(d["k"])
+        h3.rope_apply(d["q"], d["k"], d["pos"], d["tag"], d["cu_req"], frames, q_out=qr, k_out=kr)
+        outs.append(h3.varlen_attn_fwd(qr, kr, d["v"], d["cu"], 20).float())
+    assert (outs[0] - outs[1]).abs().max().item() <= 2e-2
+
+
+@pytest.mark.parametrize("cu,maxs,cap", [([0, 30, 20, 45], 30, 64),    # decreasing
+                                         ([0, 10, 30, 70], 40, 64),    # beyond capacity
+                                         ([5, 10, 30, 45], 25, 64),    # not 0-based
+                                         ([0, 10, 300, 345], 128, 400)])  # longer than max_seqlen
+def test_bad_cu_seqlens_are_reported_not_followed(h3, dev, cu, maxs, cap):
+    wl = W.random_packed(3, [cap], heads=2, head_dim=64)
+    d = _to(dev, wl)
+    o = torch.full_like(d["q"], 9.0)
+    cu_t = torch.tensor(cu, dtype=torch.int32, device=dev)
+    h3.varlen_attn_fwd(d["q"], d["k"], d["v"], cu_t, maxs, out=o)
+    assert h3.get_device_error(dev) == 3  # H3_ERR_BAD_CU_SEQLENS
+    assert h3.get_device_error(dev) == 0  # cleared by the read
+
+
+def test_all_segments_empty(h3, dev):
+    wl = W.random_packed(4, [64], heads=2, head_dim=64)
+    d = _to(dev, wl)
+    o = torch.full_like(d["q"], 2.0)
+    cu_t = torch.zeros(4, dtype=torch.int32, device=dev)
+    h3.varlen_attn_fwd(d["q"], d["k"], d["v"], cu_t, 1, out=o)
+    torch.cuda.synchronize()
+    assert h3.get_device_error(dev) == 0
+    assert torch.all(o == 2.0)
+
+
+# ---------------------------------------------------------------------------------------------
+# window partition (the shifted 3D window workload: 32x48x84 grid, 4x8x8 windows)
+# ---------------------------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def window_case():
+    return W.window_grid()
+
+
+@pytest.mark.parametrize("layer", [0, 1])
+def test_window_pack_is_exact(h3, dev, window_case, layer):
+    wl = window_case
+    shift = wl.shift if wl.layer_shifted[layer] else (0, 0, 0)
+    q, k, v = (t.to(dev) for t in wl.layers[layer])
+    perm, cu, (qp, kp, vp) = h3.window_pack(wl.grid, wl.window, shift, [q, k, v])
+    torch.cuda.synchronize()
+    p_ref, cu_ref = oracle.window_partition(wl.grid, wl.window, shift)
+    assert np.array_equal(perm.cpu().numpy(), p_ref)
+    assert np.array_equal(cu.cpu().numpy(), cu_ref)
+    assert len(cu_ref) - 1 == (528 if layer == 0 else 693)
+    idx = torch.from_numpy(p_ref.astype(np.int64)).to(dev)
+    for src, dst in ((q, qp), (k, kp), (v, vp)):
+        assert torch.equal(dst, src.index_select(0, idx))  # a gather is a pure copy
+    back = h3.window_unpack(perm, vp)
+    torch.cuda.synchronize()
+    assert torch.equal(back, v)
+
+
+@pytest.mark.parametrize("layer", [0, 1])
+def test_window_attention_layer_against_oracle(h3, dev, window_case, layer):
+    """pack -> varlen attention over window segments -> unpack, checked in original order."""
+    wl = window_case
+    shift = wl.shift if wl.layer_shifted[layer] else (0, 0, 0)
+    q, k, v = (t.to(dev) for t in wl.layers[layer])
+    perm, cu, (qp, kp, vp) = h3.window_pack(wl.grid, wl.window, shift, [q, k, v])
+    op, lse = h3.varlen_attn_fwd(qp, kp, vp, cu, 256, return_lse=True)
+    o = h3.window_unpack(perm, op)
+    torch.cuda.synchronize()
+    assert h3.get_device_error(dev) == 0
+    p_ref, cu_ref = oracle.window_partition(wl.grid, wl.window, shift)
+    nwin = len(cu_ref) - 1
+    rng = np.random.default_rng(50 + layer)
+    wins = np.unique(np.concatenate([[0, 1, nwin - 1, nwin // 2], rng.choice(nwin, 60, replace=False)]))
+    o_cpu, lse_cpu = o.cpu(), lse.cpu()
+    qc, kc, vc = wl.layers[layer]
+    for wdx in wins:
+        a, b = int(cu_ref[wdx]), int(cu_ref[wdx + 1])
+        members = p_ref[a:b].astype(np.int64)  # original rows of this window
+        ref_o, ref_lse = oracle.varlen_attention(qc[members], kc[members], vc[members], [0, b - a])
+        _close(o_cpu[members].float().numpy(), ref_o, f"window {wdx} layer {layer}")
+        _lse_close(lse_cpu[:, a:b].numpy(), ref_lse, f"window {wdx} layer {layer}")
+
+
+def test_unpack_reports_bad_perm(h3, dev):
+    n = 64
+    perm = torch.arange(n, dtype=torch.int32, device=dev)
+    perm[5] = n + 3  # out of range: the row is skipped and reported
+    src = torch.randn(n, 16, device=dev).to(torch.bfloat16)
+    dst = torch.zeros_like(src)
+    h3.window_unpack(perm, src, dst)
+    assert h3.get_device_error(dev) == 9  # H3_ERR_BAD_PERM
+    ok = torch.ones(n, dtype=torch.bool)
+    ok[5] = False
+    assert torch.equal(dst[ok.to(dev)], src[ok.to(dev)])

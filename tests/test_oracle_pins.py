@@ -406,3 +406,11 @@ def test_trim_padding_numbers(golden_dir):
     assert g["aligned_tokens"] - g["valid_tokens"] == g["padding_tokens"]
     assert 558 + 200 + 29 * 40 * 50 == g["valid_tokens"]
     assert -(-g["valid_tokens"] // 64) * 64 == g["aligned_tokens"]
+
+
+def test_rope_row_subset_matches_full():
+    wl = tiny_example()
+    full = oracle.rope_apply(wl.q, wl.pos, wl.tag, [0, 20, 45], [0.0, 119.0])
+    rows = np.array([3, 15, 19, 20, 44])
+    sub = oracle.rope_apply(wl.q, wl.pos, wl.tag, [0, 20, 45], [0.0, 119.0], rows=rows)
+    assert np.array_equal(sub, full[rows])
