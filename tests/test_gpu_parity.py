@@ -144,7 +144,15 @@ def test_end_to_end_parity_from_raw_qk(packed_case):
         vo = wl.v[a:b].double().numpy()
         ref_o, ref_lse = oracle.varlen_attention(qo, ko, vo, [0, b - a])
         _close(r["o"][a:b].float().numpy(), ref_o, f"{name} e2e seg {g}")
-        _lse_close(r["lse"][:, a:b].numpy(), ref_lse, f"{name} e2e seg {g}")
+        # The GPU rounds the rotated Q/K to bf16 (storage) before attention.  Since
+        # |d lse_i / d S_ij| = P_ij, |lse error| <= max_j |S_ij error| <=
+        # scale * 2^-8 * max_j sum_d |q_id||k_jd| (two roundings of at most 2^-9 each).
+        scale = 1.0 / np.sqrt(wl.head_dim)
+        aq, ak = np.abs(qo).transpose(1, 0, 2), np.abs(ko).transpose(1, 0, 2)  # [H, n, D]
+        bound = scale * 2.0 ** -8 * np.matmul(aq, ak.transpose(0, 2, 1)).max(axis=2)
+        got = r["lse"][:, a:b].numpy().astype(np.float64)
+        assert np.all(np.abs(got - ref_lse) <= bound + LSE_REL * np.maximum(np.abs(ref_lse), 1.0)), \
+            f"{name} e2e seg {g}: lse outside the bf16-rounding bound"
 
 
 def test_pad_rows_of_output_untouched(h3, dev):
