@@ -1,0 +1,378 @@
+#!/usr/bin/env python3
+"""Benchmark: packed varlen attention with modality-tagged 3D RoPE on GB300.
+
+One step = one pass of the hot path over one packed request: continuation time shift + tagged
+RoPE of Q and K (h3_rope_apply) and block-diagonal attention over cu_seqlens
+(h3_varlen_attn_fwd).  Default workload: the H3-shaped request of 58,758 tokens (text 558 +
+audio 200 + video 29x40x50), 40 heads x 128, bf16, segments [0,558,758,58758], capacity 58,816
+with NaN pad rows.  Metric: attention TFLOP/s = 4*H*D*sum(n_g^2) / step time.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU fp64 oracle instead (the only
+reference that exists for this method), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import resource
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "packed varlen attn TFLOP/s @58,758 tok, 40x128 bf16; % GB300 dense BF16 peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            j = json.load(f)
+        return dict(hbm_gbs=float(j["hbm_gbs"]), bf16_tflops=float(j["bf16_tflops"]),
+                    bf16_tflops_sustained=float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.reader = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+# ------------------------------------------------------------------------------------------------
+def oracle_sample_step(wl, rows):
+    """One sampled oracle step on the host cores.
+
+    The fp64 oracle rotates the sampled query rows and every key of their segment, then computes
+    attention for those rows.  The job-equivalent time charges the keys' RoPE pro rata (it is
+    shared by all rows of the segment in a full pass).  Returns
+    (attention flops, job-equivalent seconds, threads used, wall seconds).
+    """
+    import oracle
+
+    g = int(np.searchsorted(wl.cu_seqlens, rows[0], side="right")) - 1
+    a, b = int(wl.cu_seqlens[g]), int(wl.cu_seqlens[g + 1])
+    assert np.all((rows >= a) & (rows < b))
+    ru0 = resource.getrusage(resource.RUSAGE_SELF)
+    t0 = time.perf_counter()
+    ko = oracle.rope_apply(wl.k, wl.pos, wl.tag, wl.cu_requests, wl.start_frames, rows=np.arange(a, b))
+    t1 = time.perf_counter()
+    qo = oracle.rope_apply(wl.q, wl.pos, wl.tag, wl.cu_requests, wl.start_frames, rows=rows)
+    vo = wl.v[a:b].double().numpy()
+    q_seg = np.zeros((b - a, wl.num_heads, wl.head_dim))
+    q_seg[rows - a] = qo
+    oracle.varlen_attention(q_seg, ko, vo, [0, b - a], rows=rows - a)
+    t2 = time.perf_counter()
+    ru1 = resource.getrusage(resource.RUSAGE_SELF)
+    cpu = (ru1.ru_utime - ru0.ru_utime) + (ru1.ru_stime - ru0.ru_stime)
+    flops = 4.0 * wl.num_heads * wl.head_dim * (b - a) * len(rows)
+    job_s = (t2 - t1) + (t1 - t0) * len(rows) / (b - a)
+    return flops, job_s, max(1, round(cpu / (t2 - t0))), t2 - t0
+
+
+def sample_rows(wl, n_rows, seed):
+    g = int(np.argmax(np.diff(wl.cu_seqlens)))  # the long video segment
+    a, b = int(wl.cu_seqlens[g]), int(wl.cu_seqlens[g + 1])
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(np.arange(a, b), size=min(n_rows, b - a), replace=False))
+
+
+def cpu_baseline(wl, n_rows=512):
+    """The oracle on the host cores on a bounded sample (about 10-30 s); TFLOP/s."""
+    f, job_s, threads, wall = oracle_sample_step(wl, sample_rows(wl, n_rows, 1))
+    return {"value": f / job_s / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n_rows} query rows of the 58,000-row video segment x 40 heads: fp64 RoPE of those "
+                      f"rows and of all 58,000 keys (charged pro rata), then fp64 attention; "
+                      f"{f / 1e12:.3f} TFLOP, {wall:.1f} s wall; host has "
+                      f"{len(os.sched_getaffinity(0))} cores"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from workloads import h3_full_request
+
+    wl = h3_full_request()
+    n_rows = 96
+    times, flops, threads = [], 0.0, 1
+    for i in range(args.warmup + args.steps):
+        f, job_s, th, _ = oracle_sample_step(wl, sample_rows(wl, n_rows, 100 + i))
+        if i >= args.warmup:
+            times.append(job_s)
+            flops, threads = f, th
+    ms = 1e3 * float(np.mean(times))
+    value = flops / (ms / 1e3) / 1e12
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": wl.name, "tokens": wl.num_tokens, "heads": wl.num_heads,
+                       "head_dim": wl.head_dim, "cu_seqlens": [int(x) for x in wl.cu_seqlens],
+                       "sample_rows_per_step": n_rows},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"per step {n_rows} query rows of the video segment x 40 heads: "
+                                       "fp64 RoPE of those rows and of all 58,000 keys (charged pro "
+                                       "rata), then fp64 attention"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import packed_varlen_attention_modality_gb300 as h3
+    from workloads import h3_full_request
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    h3.load_library()
+    peaks = load_peaks()
+    wl = h3_full_request()
+    H, D, C, N = wl.num_heads, wl.head_dim, wl.capacity, wl.num_tokens
+    flops = wl.attention_flops()
+
+    q, k, v = (t.to(dev) for t in (wl.q, wl.k, wl.v))
+    pos = torch.from_numpy(wl.pos).to(dev)
+    tag = torch.from_numpy(wl.tag).to(dev)
+    cu = torch.from_numpy(wl.cu_seqlens).to(dev)
+    cu_req = torch.from_numpy(wl.cu_requests).to(dev)
+    frames = torch.from_numpy(wl.start_frames).to(dev)
+    qr, kr, o = torch.empty_like(q), torch.empty_like(k), torch.empty_like(q)
+    lse = torch.empty((H, C), dtype=torch.float32, device=dev)
+    max_seqlen = wl.max_seqlen
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        h3.rope_apply(q, k, pos, tag, cu_req, frames, num_tokens=N, q_out=qr, k_out=kr)
+        if ev is not None:
+            ev[1].record(stream)
+        h3.varlen_attn_fwd(qr, kr, v, cu, max_seqlen, out=o, lse=lse)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if h3.get_device_error(dev) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if h3.get_device_error(dev) != 0:
+        raise RuntimeError("device error during the timed steps")
+    rope_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    attn_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    ms_per_step = total_ms / args.steps
+    value = world * flops / (ms_per_step / 1e3) / 1e12
+
+    attn_tflops = flops / (attn_ms / 1e3) / 1e12
+    rope_bytes = 4.0 * N * H * D * 2 + 13.0 * N  # read+write Q and K (bf16) + pos (12 B) + tag (1 B)
+    rope_gbs = rope_bytes / (rope_ms / 1e3) / 1e9
+    traffic = None
+    traffic_file = os.path.join(ROOT, "profiles", "attn_fwd_dram_traffic.json")
+    if os.path.exists(traffic_file):
+        with open(traffic_file) as f:
+            tj = json.load(f)
+        if tj.get("kernel_source_sha") == _kernel_sha():
+            traffic = tj.get("dram_bytes_per_launch")
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        host = {name: t.cpu().pin_memory() for name, t in
+                (("q", q), ("k", k), ("v", v), ("pos", pos), ("tag", tag), ("cu", cu),
+                 ("cu_req", cu_req), ("frames", frames))}
+        o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        bi = sum(t.numel() * t.element_size() for t in host.values())
+        bo = o_host.numel() * o_host.element_size()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dpos, dtag, dcu = torch.empty_like(pos), torch.empty_like(tag), torch.empty_like(cu)
+        dreq, dfr = torch.empty_like(cu_req), torch.empty_like(frames)
+
+        def e2e_step():
+            for dst, name in ((dq, "q"), (dk, "k"), (dv, "v"), (dpos, "pos"), (dtag, "tag"), (dcu, "cu"),
+                              (dreq, "cu_req"), (dfr, "frames")):
+                dst.copy_(host[name], non_blocking=True)
+            h3.rope_apply(dq, dk, dpos, dtag, dreq, dfr, num_tokens=N, q_out=qr, k_out=kr)
+            h3.varlen_attn_fwd(qr, kr, dv, dcu, max_seqlen, out=o)
+            o_host.copy_(o, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(args.steps, 5))
+        s0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = s0.elapsed_time(s1) / n_e2e
+        if world > 1:
+            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * flops / (e_ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(bi),
+               "d2h_bytes_per_step": int(bo), "ms_per_step": e_ms}
+        del host, o_host, dq, dk, dv
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "tokens": N, "capacity": C, "heads": H, "head_dim": D,
+                       "cu_seqlens": [int(x) for x in wl.cu_seqlens], "attention_flop": flops,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (each of Q, K, V, O is %.0f MB > 129 MB)"
+                             % (C * H * D * 2 / 1e6)},
+            "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": attn_tflops / peaks["bf16_tflops"],
+                         "traffic": traffic, "kernel": "attn_fwd_kernel<128>",
+                         "peak_source": peaks["source"] + " bf16_tflops (burst)",
+                         "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"],
+                         "attn_ms": attn_ms},
+            "kernels": {"rope": {"ms": rope_ms, "gbs": rope_gbs, "bytes": rope_bytes,
+                                 "frac_hbm": rope_gbs / peaks["hbm_gbs"]},
+                        "attn_fwd": {"ms": attn_ms, "tflops": attn_tflops}},
+            "clocks": clocks,
+            "gpu_launches": 2 * args.steps,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def _kernel_sha():
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in ("attn_fwd_sm103.cu", "sm103_ptx.cuh"):
+        with open(os.path.join(ROOT, "packed_varlen_attention_modality_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
