@@ -41,6 +41,10 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--workload", default="h3_full_request",
+                   choices=["h3_full_request", "single_request_4k", "continuation_batch",
+                            "video_segment_16k", "window_grid"],
+                   help="h3_full_request is the metric's workload; the others are side measurements")
     return p.parse_args()
 
 
@@ -197,13 +201,16 @@ def run_reference(args, rank, world):
 # ------------------------------------------------------------------------------------------------
 def run_ours(args, rank, world, local_rank):
     import packed_varlen_attention_modality_gb300 as h3
-    from workloads import h3_full_request
+    import workloads
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     h3.load_library()
     peaks = load_peaks()
-    wl = h3_full_request()
+    if args.workload == "window_grid":
+        return run_window(args, rank, world, dev, h3, peaks)
+    headline = args.workload == "h3_full_request"
+    wl = workloads.WORKLOADS[args.workload]()
     H, D, C, N = wl.num_heads, wl.head_dim, wl.capacity, wl.num_tokens
     flops = wl.attention_flops()
 
@@ -276,7 +283,7 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
-    if not args.no_e2e:
+    if headline and not args.no_e2e:
         host = {name: t.cpu().pin_memory() for name, t in
                 (("q", q), ("k", k), ("v", v), ("pos", pos), ("tag", tag), ("cu", cu),
                  ("cu_req", cu_req), ("frames", frames))}
@@ -316,12 +323,12 @@ def run_ours(args, rank, world, local_rank):
         del host, o_host, dq, dk, dv
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if headline and rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "metric": METRIC if headline else f"packed varlen attn TFLOP/s ({wl.name})", "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl.name, "tokens": N, "capacity": C, "heads": H, "head_dim": D,
@@ -344,6 +351,95 @@ def run_ours(args, rank, world, local_rank):
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
+
+
+def run_window(args, rank, world, dev, h3, peaks):
+    """Shifted 3D window attention (32x48x84 grid, 4x8x8 windows, shift 2,4,4; 24 x 128): per step,
+    for each of the two layers (unshifted, shifted): window pack of Q/K/V -> varlen attention
+    over the window segments -> restore original order."""
+    from workloads import window_grid
+
+    wl = window_grid()
+    n, H, D = wl.num_tokens, wl.num_heads, wl.head_dim
+    layers = [tuple(t.to(dev) for t in lay) for lay in wl.layers]
+    shifts = [wl.shift if sh else (0, 0, 0) for sh in wl.layer_shifted]
+    nwins = [h3.window_count(wl.grid, wl.window, s) for s in shifts]
+    perms = [torch.empty(n, dtype=torch.int32, device=dev) for _ in shifts]
+    cus = [torch.empty(nw + 1, dtype=torch.int32, device=dev) for nw in nwins]
+    packed = [torch.empty_like(layers[0][0]) for _ in range(3)]
+    op = torch.empty_like(layers[0][0])
+    outs = [torch.empty_like(layers[0][0]) for _ in layers]
+    stream = torch.cuda.current_stream(dev)
+
+    # attention FLOPs per layer from the partition sizes (closed form per axis)
+    def axis_sizes(L, w, s):
+        return [min(L, (i + 1) * w - s) - max(0, i * w - s) for i in range((L + s + w - 1) // w)]
+    flops = []
+    for s in shifts:
+        sq = [sum(e * e for e in axis_sizes(L, w, sh)) for L, w, sh in zip(wl.grid, wl.window, s)]
+        flops.append(4.0 * H * D * sq[0] * sq[1] * sq[2])
+
+    def step(ev=None):
+        for li, (q, k, v) in enumerate(layers):
+            if ev is not None:
+                ev[li][0].record(stream)
+            h3.window_pack(wl.grid, wl.window, shifts[li], [q, k, v], perm=perms[li], cu_seqlens=cus[li],
+                           outs=packed)
+            if ev is not None:
+                ev[li][1].record(stream)
+            h3.varlen_attn_fwd(packed[0], packed[1], packed[2], cus[li], 256, out=op)
+            if ev is not None:
+                ev[li][2].record(stream)
+            h3.window_unpack(perms[li], op, outs[li])
+            if ev is not None:
+                ev[li][3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if h3.get_device_error(dev) != 0:
+        raise RuntimeError("device error during warm-up")
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in layers] for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ms_per_step = t0.elapsed_time(t1) / args.steps
+    per = {}
+    row = H * D * 2
+    pack_bytes = 2.0 * 3 * n * row + 4.0 * n   # read + write Q, K, V rows; perm
+    unpack_bytes = 2.0 * n * row + 4.0 * n
+    attn_bytes = 4.0 * n * row                   # Q, K, V read once, O written once
+    for li in range(len(layers)):
+        tp = float(np.mean([e[li][0].elapsed_time(e[li][1]) for e in evs]))
+        ta = float(np.mean([e[li][1].elapsed_time(e[li][2]) for e in evs]))
+        tu = float(np.mean([e[li][2].elapsed_time(e[li][3]) for e in evs]))
+        name = "shifted" if wl.layer_shifted[li] else "regular"
+        per[name] = {"windows": nwins[li],
+                     "pack": {"ms": tp, "gbs": pack_bytes / tp / 1e6, "frac_hbm": pack_bytes / tp / 1e6 / peaks["hbm_gbs"]},
+                     "attn": {"ms": ta, "tflops": flops[li] / ta / 1e9, "gbs": attn_bytes / ta / 1e6,
+                              "frac_hbm": attn_bytes / ta / 1e6 / peaks["hbm_gbs"],
+                              "hbm_roofline_ms": max(attn_bytes / peaks["hbm_gbs"] / 1e6,
+                                                     flops[li] / peaks["bf16_tflops"] / 1e9)},
+                     "unpack": {"ms": tu, "gbs": unpack_bytes / tu / 1e6,
+                                "frac_hbm": unpack_bytes / tu / 1e6 / peaks["hbm_gbs"]}}
+    if rank == 0:
+        value = world * sum(flops) / (ms_per_step / 1e3) / 1e12
+        print(json.dumps({
+            "metric": "shifted 3D window attention TFLOP/s (pack + attention + unpack, 2 layers)",
+            "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "tokens": n, "heads": H, "head_dim": D,
+                       "l2": "inputs larger than L2 (793 MB per tensor)"},
+            "layers": per, "clocks": clocks, "gpu_launches": 6 * args.steps}), flush=True)
 
 
 def _kernel_sha():

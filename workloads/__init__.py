@@ -244,10 +244,18 @@ def random_packed(seed: int, lengths, heads: int, head_dim: int, capacity: Optio
     return _assemble(f"random_{seed}", seed, heads, head_dim, parts, [0, N], [0.0], capacity, scale)
 
 
+def video_segment_16k(seed: int = 6) -> PackedWorkload:
+    """One 16,384-token video segment (4 latent frames of 64x64), 40 x 128: a smaller case of the
+    H3 attention shape for profiling (each of Q, K, V, O is 168 MB, larger than the 129 MB L2)."""
+    parts = [("video", 16384, _video_positions(16384, 64, 64), TAG_VIDEO)]
+    return _assemble("video_segment_16384tok_40x128", seed, 40, 128, parts, [0, 16384], [0.0], None)
+
+
 WORKLOADS = {
     "tiny_example": tiny_example,
     "single_request_4k": single_request_4k,
     "h3_full_request": h3_full_request,
     "continuation_batch": continuation_batch,
     "window_grid": window_grid,
+    "video_segment_16k": video_segment_16k,
 }
