@@ -14,14 +14,15 @@
 // otherwise leak a neighbour's or a pad row's NaN).  Overhanging query rows are never stored.
 //
 // Warp roles (384 threads = 3 warpgroups; registers moved to the softmax warpgroups with
-// setmaxnreg: 224 each for warpgroups 0 and 1, 56 for warpgroup 2):
+// setmaxnreg: 216 each for warpgroups 0 and 1, 72 for warpgroup 2):
 //   warps 0-3 / 4-7  softmax of query tile 0 / 1: thread r owns query row r = TMEM lane r and
 //              reads its full row of S = Q K^T (128 fp32) with tcgen05.ld, so the row max and
 //              row sum need no shuffles.  Running max and sum stay in fp32; P is written back to
 //              TMEM over S as bf16 (the A operand of the PV product); O is rescaled in TMEM only
 //              when the running max grows by more than 2^8; the epilogue normalises O and
 //              stores it (and the LSE).
-//   warp 8     TMA producer: Q tiles once, then K and V tiles through 2-stage rings.
+//   warp 8     TMA producer: Q tiles once, then K and V tiles through rings (3 K / 2 V stages
+//              at D = 128).
 //   warps 10-11 idle (they complete warpgroup 2).
 //   warp 9     MMA issuer (one thread).  Order per key tile j:
 //                PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
@@ -41,8 +42,8 @@ constexpr int kBlockM = 128;          // query rows per tile
 constexpr int kBlockN = 128;          // keys per tile
 constexpr int kTilesPerCta = 2;       // query tiles per CTA
 constexpr int kThreads = 384;
-constexpr int kRegsSoftmax = 224;  // 128 * (224 + 224 + 56) = 384 * 168 registers at launch
-constexpr int kRegsOther = 56;
+constexpr int kRegsSoftmax = 216;  // 128 * (216 + 216 + 72) = 384 * 168 registers at launch
+constexpr int kRegsOther = 72;
 constexpr int kTmemCols = 512;
 constexpr int kColO = 0;              // O of tile t at kColO + 128 t
 constexpr int kColS = 256;            // S / P of tile t at kColS + 128 t
@@ -53,12 +54,14 @@ struct Cfg {
   static constexpr int kBoxes = D / 64;               // 64-column (128-byte) swizzle boxes
   static constexpr int kTileBytes = kBlockM * D * 2;  // one Q, K or V tile
   static constexpr int kBoxBytes = kBlockM * 128;     // one 128-row box
-  static constexpr int kStages = (D == 128) ? 2 : 4;  // K and V ring depth
-  // q_full[2], k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_final[2],
-  // drain
-  static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 2 + 1;
-  static constexpr int kSmemBytes =
-      1024 /*alignment slack*/ + kTileBytes * (kTilesPerCta + 2 * kStages) + kNumBars * 8 + 16;
+  static constexpr int kStagesK = (D == 128) ? 3 : 4;  // K ring depth
+  static constexpr int kStagesV = (D == 128) ? 2 : 4;  // V ring depth
+  // q_full[2], k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2], p_full[2],
+  // o_final[2], drain
+  static constexpr int kNumBars = 2 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 1;
+  static constexpr int kSmemBytes = 1024 /*alignment slack*/ +
+                                    kTileBytes * (kTilesPerCta + kStagesK + kStagesV) +
+                                    kNumBars * 8 + 16;
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(kBlockM, kBlockN, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, true);
 };
@@ -71,25 +74,27 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 float* __restrict__ lse, const int32_t* __restrict__ cu_seqlens, int capacity,
                 int num_heads, float scale, float scale_log2, unsigned int* err) {
   using C = Cfg<D>;
-  constexpr int S = C::kStages;
+  constexpr int SK = C::kStagesK;
+  constexpr int SV = C::kStagesV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;                                  // 2 tiles
-  uint8_t* sK = sQ + kTilesPerCta * C::kTileBytes;     // S tiles
-  uint8_t* sV = sK + S * C::kTileBytes;                // S tiles
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + S * C::kTileBytes);
+  uint8_t* sK = sQ + kTilesPerCta * C::kTileBytes;     // SK tiles
+  uint8_t* sV = sK + SK * C::kTileBytes;               // SV tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + SV * C::kTileBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
 
   auto bar_qfull = [&](int t) { return smem_u32(&bars[t]); };
+  constexpr int kB = 2 + 2 * SK + 2 * SV;  // first per-tile barrier after the rings
   auto bar_kfull = [&](int s) { return smem_u32(&bars[2 + s]); };
-  auto bar_vfull = [&](int s) { return smem_u32(&bars[2 + S + s]); };
-  auto bar_kempty = [&](int s) { return smem_u32(&bars[2 + 2 * S + s]); };
-  auto bar_vempty = [&](int s) { return smem_u32(&bars[2 + 3 * S + s]); };
-  auto bar_sfull = [&](int t) { return smem_u32(&bars[2 + 4 * S + t]); };
-  auto bar_pfull = [&](int t) { return smem_u32(&bars[4 + 4 * S + t]); };
-  auto bar_ofinal = [&](int t) { return smem_u32(&bars[6 + 4 * S + t]); };
-  const uint32_t bar_drain = smem_u32(&bars[8 + 4 * S]);
+  auto bar_kempty = [&](int s) { return smem_u32(&bars[2 + SK + s]); };
+  auto bar_vfull = [&](int s) { return smem_u32(&bars[2 + 2 * SK + s]); };
+  auto bar_vempty = [&](int s) { return smem_u32(&bars[2 + 2 * SK + SV + s]); };
+  auto bar_sfull = [&](int t) { return smem_u32(&bars[kB + t]); };
+  auto bar_pfull = [&](int t) { return smem_u32(&bars[kB + 2 + t]); };
+  auto bar_ofinal = [&](int t) { return smem_u32(&bars[kB + 4 + t]); };
+  const uint32_t bar_drain = smem_u32(&bars[kB + 6]);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -131,10 +136,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       mbar_init(bar_pfull(t), 128);
       mbar_init(bar_ofinal(t), 1);
     }
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < SK; ++s) {
       mbar_init(bar_kfull(s), 1);
-      mbar_init(bar_vfull(s), 1);
       mbar_init(bar_kempty(s), 1);
+    }
+    for (int s = 0; s < SV; ++s) {
+      mbar_init(bar_vfull(s), 1);
       mbar_init(bar_vempty(s), 1);
     }
     mbar_init(bar_drain, 1);
@@ -163,22 +170,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                         q0 + t * kBlockM, bar_qfull(t));
         }
         for (int j = 0; j < nkv; ++j) {
-          const int s = j % S;
-          const uint32_t ph = (j / S) & 1;
           const int row = seg_start + j * kBlockN;
-          ok = mbar_wait(bar_kempty(s), ph ^ 1);
+          const int s = j % SK;
+          ok = mbar_wait(bar_kempty(s), ((j / SK) & 1) ^ 1);
           if (!ok) break;
           mbar_arrive_expect_tx(bar_kfull(s), C::kTileBytes);
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(smem_u32(sK + s * C::kTileBytes + b * C::kBoxBytes), &tmap_k, b * 64, head,
                         row, bar_kfull(s));
           issued_k = j + 1;
-          ok = mbar_wait(bar_vempty(s), ph ^ 1);
+          const int v = j % SV;
+          ok = mbar_wait(bar_vempty(v), ((j / SV) & 1) ^ 1);
           if (!ok) break;
-          mbar_arrive_expect_tx(bar_vfull(s), C::kTileBytes);
+          mbar_arrive_expect_tx(bar_vfull(v), C::kTileBytes);
           for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(smem_u32(sV + s * C::kTileBytes + b * C::kBoxBytes), &tmap_v, b * 64, head,
-                        row, bar_vfull(s));
+            tma_load_3d(smem_u32(sV + v * C::kTileBytes + b * C::kBoxBytes), &tmap_v, b * 64, head,
+                        row, bar_vfull(v));
           issued_v = j + 1;
         }
         if (!ok) record_error(err, kErrTimeout);
@@ -186,10 +193,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         // The last S loads of each kind sit on distinct stages, so each stage's latest phase is
         // the one to wait for (already complete in the normal path).
         for (int t = 0; t < (has1 ? 2 : 1); ++t) mbar_wait(bar_qfull(t), 0);
-        for (int j = issued_k - 1; j >= 0 && j >= issued_k - S; --j)
-          mbar_wait(bar_kfull(j % S), (j / S) & 1);
-        for (int j = issued_v - 1; j >= 0 && j >= issued_v - S; --j)
-          mbar_wait(bar_vfull(j % S), (j / S) & 1);
+        for (int j = issued_k - 1; j >= 0 && j >= issued_k - SK; --j)
+          mbar_wait(bar_kfull(j % SK), (j / SK) & 1);
+        for (int j = issued_v - 1; j >= 0 && j >= issued_v - SV; --j)
+          mbar_wait(bar_vfull(j % SV), (j / SV) & 1);
       }
     } else if (warp == 9) {
       // ================= MMA issuer =================
@@ -202,7 +209,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const uint32_t d = tmem + kColS + 128 * t;
         const uint32_t qa = qa0 + t * C::kTileBytes;
         const uint32_t kb = smem_u32(sK + s * C::kTileBytes);
-  #pragma unroll
+#pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
           mma_ss(d, sw128_desc(qa + off, 16, 1024), sw128_desc(kb + off, 16, 1024), C::kIdescQK,
@@ -213,7 +220,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       auto issue_pv = [&](int t, int s, bool first) {  // O_t += P_t V_s
         const uint32_t p = tmem + kColS + 128 * t;
         const uint32_t vb = smem_u32(sV + s * C::kTileBytes);
-  #pragma unroll
+#pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
           // 16 keys per MMA: 8 TMEM columns of packed bf16 P; 16 rows (2 KB) of V
           mma_ts(tmem + kColO + 128 * t, p + kk * 8, sw128_desc(vb + kk * 2048, C::kBoxBytes, 1024),
@@ -233,10 +240,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         __syncwarp();
       }
       for (int j = 0; j < nkv && ok; ++j) {
-        const int sv = j % S;
+        const int sv = j % SV;
         const bool more = j + 1 < nkv;
-        const int sk = (j + 1) % S;
-        ok = wait_all(bar_vfull(sv), (j / S) & 1);
+        const int sk = (j + 1) % SK;
+        ok = wait_all(bar_vfull(sv), (j / SV) & 1);
         if (!ok) break;
         if (j == nkv - 1 && kv_last_valid < kBlockN) {
           // Zero the value rows past the segment end (rows are 128 B per box; the swizzle only
@@ -255,7 +262,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         // tile 0: PV0_j, then S0_{j+1}
         ok = wait_all(bar_pfull(0), j & 1);
         if (!ok) break;
-        if (more) ok = wait_all(bar_kfull(sk), ((j + 1) / S) & 1);
+        if (more) ok = wait_all(bar_kfull(sk), ((j + 1) / SK) & 1);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
@@ -319,19 +326,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         tmem_ld_wait();
         tmem_reg_fence<128>(sr);
         float s[128];
-  #pragma unroll
+#pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
         if (j == nkv - 1 && kv_last_valid < kBlockN) {
           // keys past the segment end: -inf by select, so a NaN/Inf score there is discarded
-  #pragma unroll
+#pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (c < kv_last_valid) ? s[c] : -INFINITY;
         }
-        // row max: four independent chains of 3-input max
+        // row max: four chains, chain u over columns u, u+4, ...: seeded with s[0..3], 3-input
+        // steps over columns 4..123, then 124..127
         float m4[4] = {s[0], s[1], s[2], s[3]};
-  #pragma unroll
-        for (int c = 4; c < 128; c += 8)
-  #pragma unroll
+#pragma unroll
+        for (int c = 4; c < 124; c += 8)
+#pragma unroll
           for (int u = 0; u < 4; ++u) m4[u] = fmax3(m4[u], s[c + u], s[c + 4 + u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) m4[u] = fmaxf(m4[u], s[124 + u]);
         const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         float alpha = 1.f;
         bool rescale = false;
@@ -343,13 +353,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
         if (__any_sync(0xffffffffu, rescale)) {
           // O_t is stable: PV_t,{j-1} was issued before S_t,j, whose completion we observed.
-  #pragma unroll 1
+#pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t orr[32];
             tmem_ld32(o_addr + c0, orr);
             tmem_ld_wait();
             tmem_reg_fence<32>(orr);
-  #pragma unroll
+#pragma unroll
             for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
             tmem_st32(o_addr + c0, orr);
           }
@@ -358,7 +368,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const float2 nm2 = make_float2(-mb, -mb);
         float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
         uint32_t p[64];
-  #pragma unroll
+#pragma unroll
         for (int c = 0; c < 64; ++c) {
           const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), c2, nm2);
           const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
@@ -385,20 +395,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const bool valid = q_row < seg_end;
         const float inv_l = 1.f / l;
         __nv_bfloat16* orow = out + (static_cast<size_t>(q_row) * num_heads + head) * D;
-  #pragma unroll 1
+#pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t orr[32];
           tmem_ld32(o_addr + c0, orr);
           tmem_ld_wait();
           tmem_reg_fence<32>(orr);
           uint32_t pk[16];
-  #pragma unroll
+#pragma unroll
           for (int c = 0; c < 16; ++c)
             pk[c] = pack_bf16x2(__uint_as_float(orr[2 * c]) * inv_l,
                                 __uint_as_float(orr[2 * c + 1]) * inv_l);
           if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-  #pragma unroll
+#pragma unroll
             for (int c = 0; c < 4; ++c)
               dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
           }
