@@ -223,6 +223,8 @@ def run_ours(args, rank, world, local_rank):
     qr, kr, o = torch.empty_like(q), torch.empty_like(k), torch.empty_like(q)
     lse = torch.empty((H, C), dtype=torch.float32, device=dev)
     max_seqlen = wl.max_seqlen
+    ws = torch.empty(max(16, h3.varlen_attn_workspace_size(wl.num_segments, H, max_seqlen, D)),
+                     dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(ev=None):
@@ -231,7 +233,7 @@ def run_ours(args, rank, world, local_rank):
         h3.rope_apply(q, k, pos, tag, cu_req, frames, num_tokens=N, q_out=qr, k_out=kr)
         if ev is not None:
             ev[1].record(stream)
-        h3.varlen_attn_fwd(qr, kr, v, cu, max_seqlen, out=o, lse=lse)
+        h3.varlen_attn_fwd(qr, kr, v, cu, max_seqlen, out=o, lse=lse, workspace=ws)
         if ev is not None:
             ev[2].record(stream)
 
@@ -299,7 +301,7 @@ def run_ours(args, rank, world, local_rank):
                               (dreq, "cu_req"), (dfr, "frames")):
                 dst.copy_(host[name], non_blocking=True)
             h3.rope_apply(dq, dk, dpos, dtag, dreq, dfr, num_tokens=N, q_out=qr, k_out=kr)
-            h3.varlen_attn_fwd(qr, kr, dv, dcu, max_seqlen, out=o)
+            h3.varlen_attn_fwd(qr, kr, dv, dcu, max_seqlen, out=o, workspace=ws)
             o_host.copy_(o, non_blocking=True)
 
         e2e_step()
@@ -368,6 +370,8 @@ def run_window(args, rank, world, dev, h3, peaks):
     cus = [torch.empty(nw + 1, dtype=torch.int32, device=dev) for nw in nwins]
     packed = [torch.empty_like(layers[0][0]) for _ in range(3)]
     op = torch.empty_like(layers[0][0])
+    wss = [torch.empty(h3.varlen_attn_workspace_size(nw, H, 256, D), dtype=torch.uint8, device=dev)
+           for nw in nwins]
     outs = [torch.empty_like(layers[0][0]) for _ in layers]
     stream = torch.cuda.current_stream(dev)
 
@@ -387,7 +391,7 @@ def run_window(args, rank, world, dev, h3, peaks):
                            outs=packed)
             if ev is not None:
                 ev[li][1].record(stream)
-            h3.varlen_attn_fwd(packed[0], packed[1], packed[2], cus[li], 256, out=op)
+            h3.varlen_attn_fwd(packed[0], packed[1], packed[2], cus[li], 256, out=op, workspace=wss[li])
             if ev is not None:
                 ev[li][2].record(stream)
             h3.window_unpack(perms[li], op, outs[li])

@@ -110,7 +110,9 @@ H3_API h3_status h3_rope_apply(const void* q_in, void* q_out, const void* k_in, 
                         const int32_t* cu_requests, int32_t num_requests,
                         const float* start_frames, const h3_rope_cfg* cfg, h3_stream_t stream);
 
-/* Bytes of device workspace h3_varlen_attn_fwd needs for these sizes (may be 0). */
+/* Bytes of device workspace h3_varlen_attn_fwd needs for these sizes: the work plan written by
+ * the call itself (segment order and item prefix, 8 bytes per segment, plus a 16-byte header),
+ * rounded up to 256.  0 when num_segments <= 0. */
 H3_API size_t h3_varlen_attn_workspace_size(int32_t num_segments, int32_t num_heads,
                                      int32_t max_seqlen, int32_t head_dim);
 
@@ -127,10 +129,13 @@ H3_API size_t h3_varlen_attn_workspace_size(int32_t num_segments, int32_t num_he
  * lse         : device fp32 [H, capacity] (natural log) or NULL.
  * cu_seqlens  : device int32 [num_segments + 1]; must start at 0, not decrease, end <= capacity.
  *               Empty segments are allowed.
- * max_seqlen  : host upper bound on the longest segment (sizes the launch).
+ * max_seqlen  : host upper bound on the longest segment.  A longer segment is still computed in
+ *               full but reported as H3_ERR_BAD_CU_SEQLENS.
  * softmax_scale: <= 0 selects 1/sqrt(head_dim).
  * workspace   : device scratch of h3_varlen_attn_workspace_size() bytes (16-byte aligned), or
- *               NULL when that size is 0.  Contents need not be initialised.
+ *               NULL when that size is 0.  Contents need not be initialised; the call rewrites
+ *               them.  Calls that may run at the same time (other streams) need separate
+ *               workspaces.
  * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG, H3_ERR_UNSUPPORTED, H3_ERR_MISALIGNED,
  *         H3_ERR_WORKSPACE, H3_ERR_CUDA; device-side H3_ERR_BAD_CU_SEQLENS / H3_ERR_TIMEOUT.
  */

@@ -5,31 +5,45 @@
 // sub-sequence g softmax-normalises over the keys of g only (no causal mask: the worked
 // example's token 15 sees keys 10..29).  Sec. 6: rows past the valid length never take part.
 //
-// Work unit: one CTA = two 128-row query tiles (256 rows) of one segment and one head; both
-// tiles stream the same key/value tiles, so each K/V tile staged in shared memory feeds twice
-// the tensor-core work.  No tile crosses a segment boundary: query and key/value tiles start at
-// the segment's first row (TMA boxes may start at any row), so only the segment's LAST key tile
-// can overhang.  On that tile the overhanging key columns are masked to -inf by select, and
-// the overhanging value rows are zeroed in shared memory before the PV product (0 * NaN would
+// Work item: two 128-row query tiles (256 rows) of one segment and one head; both tiles stream
+// the same key/value tiles, so each K/V tile staged in shared memory feeds twice the
+// tensor-core work.  No tile crosses a segment boundary: query and key/value tiles start at the
+// segment's first row (TMA boxes may start at any row), so only the segment's LAST key tile can
+// overhang.  On that tile the overhanging key columns are masked to -inf by select, and the
+// overhanging value rows are zeroed in shared memory before the PV product (0 * NaN would
 // otherwise leak a neighbour's or a pad row's NaN).  Overhanging query rows are never stored.
 //
+// Scheduling: a one-CTA plan kernel validates cu_seqlens, orders the segments longest first
+// (up to kSortMax segments; beyond that in given order) and writes the exclusive prefix of work
+// items per segment into the caller's workspace.  CTA c takes items c, c + G, c + 2G, ... (G =
+// grid size); its TMA warp decodes each item and hands it to the other roles through a 2-slot
+// ring in shared memory.  For short segments (max_seqlen <= kPersistMaxSeqlen) the grid is one
+// CTA per SM and each CTA loops over items: the K/V ring, the Q reload (after the item's last
+// QK^T) and the epilogue (before the next item's first PV) overlap consecutive items, which pays
+// for 3D windows of a few hundred rows.  For long segments the grid has one CTA per item (set
+// up per item costs little against hundreds of key tiles, and measured faster there).  Items of
+// one segment are numbered head-major, so the CTAs working at one time share a head's K/V in L2.
+//
 // Warp roles (384 threads = 3 warpgroups; registers moved to the softmax warpgroups with
-// setmaxnreg: 216 each for warpgroups 0 and 1, 72 for warpgroup 2):
+// setmaxnreg: 200 each for warpgroups 0 and 1, 104 for warpgroup 2):
 //   warps 0-3 / 4-7  softmax of query tile 0 / 1: thread r owns query row r = TMEM lane r and
 //              reads its full row of S = Q K^T (128 fp32) with tcgen05.ld, so the row max and
 //              row sum need no shuffles.  Running max and sum stay in fp32; P is written back to
 //              TMEM over S as bf16 (the A operand of the PV product); O is rescaled in TMEM only
 //              when the running max grows by more than 2^8; the epilogue normalises O and
 //              stores it (and the LSE).
-//   warp 8     TMA producer: Q tiles once, then K and V tiles through rings (3 K / 2 V stages
-//              at D = 128).
-//   warps 10-11 idle (they complete warpgroup 2).
+//   warp 8     scheduler + TMA producer: Q tiles once per item, then K and V tiles through
+//              rings (3 K / 2 V stages at D = 128) that run on across items.
 //   warp 9     MMA issuer (one thread).  Order per key tile j:
 //                PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
 //              so while softmax 0 works on S0_{j+1} the tensor core runs PV1_j and S1_{j+1},
 //              and vice versa (ping-pong).  Because S_t,{j+1} is issued after PV_t,j, seeing
 //              S_t,{j+1} complete also means O_t is stable for an in-place rescale.
+//   warps 10-11 idle (they complete warpgroup 2).
 // TMEM (512 columns): O0 [0,128), O1 [128,256), S0/P0 [256,384), S1/P1 [384,512).
+//
+// Barrier phases run on across items: every role counts its own completions and derives each
+// wait's parity from them; no waiter can fall more than one phase behind its barrier.
 #include <cuda_bf16.h>
 
 #include "h3_internal.h"
@@ -40,14 +54,124 @@ namespace {
 
 constexpr int kBlockM = 128;          // query rows per tile
 constexpr int kBlockN = 128;          // keys per tile
-constexpr int kTilesPerCta = 2;       // query tiles per CTA
+constexpr int kTilesPerItem = 2;      // query tiles per work item
+constexpr int kRowsPerItem = kTilesPerItem * kBlockM;
 constexpr int kThreads = 384;
-constexpr int kRegsSoftmax = 216;  // 128 * (216 + 216 + 72) = 384 * 168 registers at launch
-constexpr int kRegsOther = 72;
+constexpr int kRegsSoftmax = 200;  // 128 * (200 + 200 + 104) = 384 * 168 registers at launch
+constexpr int kRegsOther = 104;
 constexpr int kTmemCols = 512;
 constexpr int kColO = 0;              // O of tile t at kColO + 128 t
 constexpr int kColS = 256;            // S / P of tile t at kColS + 128 t
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the running max grows by > 2^8
+constexpr int kPlanThreads = 1024;
+constexpr int kSortMax = 256;         // segments ordered longest-first up to this count
+constexpr int kWsHeader = 4;          // workspace words: (spare), total items, 2 spare
+constexpr int kPersistMaxSeqlen = 2048;  // loop over items per CTA up to this segment length
+
+// Workspace (uint32 words): [1] total items, [kWsHeader, +S) segment order,
+// [kWsHeader + S, +S+1) exclusive prefix of items in that order.
+__host__ __device__ constexpr size_t workspace_words(int num_segments) {
+  return kWsHeader + 2 * static_cast<size_t>(num_segments) + 1;
+}
+
+struct WorkDesc {
+  int seg_start;
+  int seg_len;  // < 0: no more work
+  int head;
+  int q0;
+};
+
+__device__ __forceinline__ int checked_len(const int32_t* __restrict__ cu, int g, int capacity,
+                                           int max_seqlen, unsigned int* err) {
+  const int a = cu[g], b = cu[g + 1];
+  if (a < 0 || b < a || b > capacity || (g == 0 && a != 0)) {
+    record_error(err, kErrBadCuSeqlens);
+    return 0;  // an invalid segment produces nothing
+  }
+  if (b - a > max_seqlen) record_error(err, kErrBadCuSeqlens);  // computed all the same
+  return b - a;
+}
+
+__device__ __forceinline__ uint32_t items_of(int len, int heads) {
+  return static_cast<uint32_t>((len + kRowsPerItem - 1) / kRowsPerItem) * heads;
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+attn_plan_kernel(const int32_t* __restrict__ cu, int num_segments, int capacity, int max_seqlen,
+                 int num_heads, uint32_t* __restrict__ ws, unsigned int* err) {
+  __shared__ int s_len[kSortMax];
+  __shared__ uint32_t s_part[kPlanThreads];
+  const int S = num_segments;
+  const int tid = threadIdx.x;
+  uint32_t* order = ws + kWsHeader;
+  uint32_t* prefix = ws + kWsHeader + S;
+  const bool sorted = S <= kSortMax;
+
+  if (sorted) {
+    // longest first, ties by position (a stable order): rank = number of segments before it
+    for (int g = tid; g < S; g += kPlanThreads)
+      s_len[g] = checked_len(cu, g, capacity, max_seqlen, err);
+    __syncthreads();
+    for (int g = tid; g < S; g += kPlanThreads) {
+      int rank = 0;
+      for (int h = 0; h < S; ++h) rank += (s_len[h] > s_len[g]) || (s_len[h] == s_len[g] && h < g);
+      order[rank] = static_cast<uint32_t>(g);
+    }
+  } else {
+    for (int g = tid; g < S; g += kPlanThreads) order[g] = static_cast<uint32_t>(g);
+  }
+  __syncthreads();
+  auto len_of = [&](int g) {
+    return sorted ? s_len[g] : checked_len(cu, g, capacity, max_seqlen, err);
+  };
+
+  // exclusive prefix of items over the ordered segments: per-thread chunks + block scan
+  const int chunk = (S + kPlanThreads - 1) / kPlanThreads;
+  const int lo = min(S, tid * chunk), hi = min(S, lo + chunk);
+  uint32_t local = 0;
+  for (int i = lo; i < hi; ++i) local += items_of(len_of(static_cast<int>(order[i])), num_heads);
+  s_part[tid] = local;
+  __syncthreads();
+  for (int off = 1; off < kPlanThreads; off <<= 1) {  // inclusive Hillis-Steele scan
+    const uint32_t v = tid >= off ? s_part[tid - off] : 0u;
+    __syncthreads();
+    s_part[tid] += v;
+    __syncthreads();
+  }
+  uint32_t run = tid ? s_part[tid - 1] : 0u;
+  for (int i = lo; i < hi; ++i) {
+    prefix[i] = run;
+    run += items_of(len_of(static_cast<int>(order[i])), num_heads);
+  }
+  if (tid == kPlanThreads - 1) {
+    prefix[S] = s_part[kPlanThreads - 1];
+    ws[1] = s_part[kPlanThreads - 1];
+  }
+}
+
+// Item index -> work descriptor (binary search of the ordered prefix).
+__device__ __forceinline__ WorkDesc decode_item(uint32_t item, const uint32_t* __restrict__ ws,
+                                                const int32_t* __restrict__ cu, int S,
+                                                int num_heads) {
+  const uint32_t* order = ws + kWsHeader;
+  const uint32_t* prefix = ws + kWsHeader + S;
+  int lo = 0, hi = S - 1;  // last i with prefix[i] <= item (empty segments repeat a value)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  const int g = static_cast<int>(order[lo]);
+  const int a = cu[g], len = cu[g + 1] - a;
+  const uint32_t pairs = static_cast<uint32_t>((len + kRowsPerItem - 1) / kRowsPerItem);
+  const uint32_t local = item - prefix[lo];
+  WorkDesc d;
+  d.seg_start = a;
+  d.seg_len = len;
+  d.head = static_cast<int>(local / pairs);
+  d.q0 = a + static_cast<int>(local % pairs) * kRowsPerItem;
+  (void)num_heads;
+  return d;
+}
 
 template <int D>
 struct Cfg {
@@ -56,12 +180,12 @@ struct Cfg {
   static constexpr int kBoxBytes = kBlockM * 128;     // one 128-row box
   static constexpr int kStagesK = (D == 128) ? 3 : 4;  // K ring depth
   static constexpr int kStagesV = (D == 128) ? 2 : 4;  // V ring depth
-  // q_full[2], k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2], p_full[2],
-  // o_final[2], drain
-  static constexpr int kNumBars = 2 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 1;
+  // q_full[2], q_empty, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
+  // p_full[2], o_final[2], o_empty[2], w_full[2], w_empty[2], drain
+  static constexpr int kNumBars = 3 + 2 * kStagesK + 2 * kStagesV + 12 + 1;
   static constexpr int kSmemBytes = 1024 /*alignment slack*/ +
-                                    kTileBytes * (kTilesPerCta + kStagesK + kStagesV) +
-                                    kNumBars * 8 + 16;
+                                    kTileBytes * (kTilesPerItem + kStagesK + kStagesV) +
+                                    kNumBars * 8 + 16 /*TMEM slot*/ + 2 * 16 /*work ring*/;
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(kBlockM, kBlockN, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, true);
 };
@@ -71,8 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, __nv_bfloat16* __restrict__ out,
-                float* __restrict__ lse, const int32_t* __restrict__ cu_seqlens, int capacity,
-                int num_heads, float scale, float scale_log2, unsigned int* err) {
+                float* __restrict__ lse, const int32_t* __restrict__ cu_seqlens, int num_segments,
+                int capacity, int num_heads, float scale, float scale_log2,
+                uint32_t* __restrict__ ws, unsigned int* err) {
   using C = Cfg<D>;
   constexpr int SK = C::kStagesK;
   constexpr int SV = C::kStagesV;
@@ -80,50 +205,33 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;                                  // 2 tiles
-  uint8_t* sK = sQ + kTilesPerCta * C::kTileBytes;     // SK tiles
+  uint8_t* sK = sQ + kTilesPerItem * C::kTileBytes;    // SK tiles
   uint8_t* sV = sK + SK * C::kTileBytes;               // SV tiles
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + SV * C::kTileBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  WorkDesc* work = reinterpret_cast<WorkDesc*>(tmem_slot + 4);  // 2-slot ring
 
+  constexpr int kB = 3 + 2 * SK + 2 * SV;  // first per-tile barrier after the rings
   auto bar_qfull = [&](int t) { return smem_u32(&bars[t]); };
-  constexpr int kB = 2 + 2 * SK + 2 * SV;  // first per-tile barrier after the rings
-  auto bar_kfull = [&](int s) { return smem_u32(&bars[2 + s]); };
-  auto bar_kempty = [&](int s) { return smem_u32(&bars[2 + SK + s]); };
-  auto bar_vfull = [&](int s) { return smem_u32(&bars[2 + 2 * SK + s]); };
-  auto bar_vempty = [&](int s) { return smem_u32(&bars[2 + 2 * SK + SV + s]); };
+  const uint32_t bar_qempty = smem_u32(&bars[2]);
+  auto bar_kfull = [&](int s) { return smem_u32(&bars[3 + s]); };
+  auto bar_kempty = [&](int s) { return smem_u32(&bars[3 + SK + s]); };
+  auto bar_vfull = [&](int s) { return smem_u32(&bars[3 + 2 * SK + s]); };
+  auto bar_vempty = [&](int s) { return smem_u32(&bars[3 + 2 * SK + SV + s]); };
   auto bar_sfull = [&](int t) { return smem_u32(&bars[kB + t]); };
   auto bar_pfull = [&](int t) { return smem_u32(&bars[kB + 2 + t]); };
   auto bar_ofinal = [&](int t) { return smem_u32(&bars[kB + 4 + t]); };
-  const uint32_t bar_drain = smem_u32(&bars[kB + 6]);
+  auto bar_oempty = [&](int t) { return smem_u32(&bars[kB + 6 + t]); };
+  auto bar_wfull = [&](int i) { return smem_u32(&bars[kB + 8 + i]); };
+  auto bar_wempty = [&](int i) { return smem_u32(&bars[kB + 10 + i]); };
+  const uint32_t bar_drain = smem_u32(&bars[kB + 12]);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int pair = blockIdx.x;  // query tiles 2*pair and 2*pair+1 of the segment
-  const int head = blockIdx.y;
-  const int seg = blockIdx.z;
 
   // A wait that timed out earlier (recorded, not yet read) means the machinery is not healthy:
-  // every later CTA leaves at once instead of running into its own 2-second waits.
+  // leave at once instead of running into 2-second waits again.
   if (err != nullptr && *reinterpret_cast<volatile unsigned int*>(err) == kErrTimeout) return;
-
-  // ---- segment bounds (device-side validation; uniform across the CTA) ----
-  const int seg_start = cu_seqlens[seg];
-  const int seg_end = cu_seqlens[seg + 1];
-  const bool bad = seg_start < 0 || seg_end < seg_start || seg_end > capacity ||
-                   (seg == 0 && seg_start != 0);
-  if (bad) {
-    if (threadIdx.x == 0 && pair == 0 && head == 0) record_error(err, kErrBadCuSeqlens);
-    return;
-  }
-  const int seg_len = seg_end - seg_start;
-  if (pair == static_cast<int>(gridDim.x) - 1 && threadIdx.x == 0 && head == 0 &&
-      seg_len > static_cast<int>(gridDim.x) * kTilesPerCta * kBlockM)
-    record_error(err, kErrBadCuSeqlens);  // max_seqlen smaller than a segment
-  const int q0 = seg_start + pair * kTilesPerCta * kBlockM;
-  if (q0 >= seg_end) return;
-  const bool has1 = q0 + kBlockM < seg_end;  // second query tile present
-  const int nkv = (seg_len + kBlockN - 1) / kBlockN;
-  const int kv_last_valid = seg_len - (nkv - 1) * kBlockN;  // keys in the last tile, 1..128
 
   // ---- setup: barriers (warp 8), TMEM (warp 9) ----
   if (warp == 8 && lane == 0) {
@@ -135,7 +243,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       mbar_init(bar_sfull(t), 1);
       mbar_init(bar_pfull(t), 128);
       mbar_init(bar_ofinal(t), 1);
+      mbar_init(bar_oempty(t), 128);
+      mbar_init(bar_wfull(t), 1);
+      mbar_init(bar_wempty(t), 9);  // the MMA warp + lane 0 of each of the 8 softmax warps
     }
+    mbar_init(bar_qempty, 1);
     for (int s = 0; s < SK; ++s) {
       mbar_init(bar_kfull(s), 1);
       mbar_init(bar_kempty(s), 1);
@@ -159,44 +271,75 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
   if (warp >= 8) {
     setmaxnreg_dec<kRegsOther>();
     if (warp == 8) {
-      // ================= TMA producer =================
+      // ================= scheduler + TMA producer =================
       if (lane == 0) {
-        int issued_k = 0, issued_v = 0;
+        const uint32_t total = ws[1];
+        uint32_t kt = 0, vt = 0;  // K / V tiles loaded so far (positions in the rings)
+        uint32_t qn[2] = {0u, 0u};  // Q tiles loaded so far, per tile slot
         bool ok = true;
-        for (int t = 0; t < (has1 ? 2 : 1); ++t) {
-          mbar_arrive_expect_tx(bar_qfull(t), C::kTileBytes);
-          for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(smem_u32(sQ + t * C::kTileBytes + b * C::kBoxBytes), &tmap_q, b * 64, head,
-                        q0 + t * kBlockM, bar_qfull(t));
-        }
-        for (int j = 0; j < nkv; ++j) {
-          const int row = seg_start + j * kBlockN;
-          const int s = j % SK;
-          ok = mbar_wait(bar_kempty(s), ((j / SK) & 1) ^ 1);
+        for (int k = 0; ok; ++k) {
+          const uint32_t item = blockIdx.x + static_cast<uint32_t>(k) * gridDim.x;
+          WorkDesc d;
+          if (item < total) {
+            d = decode_item(item, ws, cu_seqlens, num_segments, num_heads);
+          } else {
+            d.seg_start = 0;
+            d.seg_len = -1;
+            d.head = 0;
+            d.q0 = 0;
+          }
+          ok = mbar_wait(bar_wempty(k & 1), ((k >> 1) & 1) ^ 1);
           if (!ok) break;
-          mbar_arrive_expect_tx(bar_kfull(s), C::kTileBytes);
-          for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(smem_u32(sK + s * C::kTileBytes + b * C::kBoxBytes), &tmap_k, b * 64, head,
-                        row, bar_kfull(s));
-          issued_k = j + 1;
-          const int v = j % SV;
-          ok = mbar_wait(bar_vempty(v), ((j / SV) & 1) ^ 1);
+          work[k & 1] = d;
+          mbar_arrive(bar_wfull(k & 1));
+          if (d.seg_len < 0) break;
+          const int seg_end = d.seg_start + d.seg_len;
+          const bool has1 = d.q0 + kBlockM < seg_end;
+          const int nkv = (d.seg_len + kBlockN - 1) / kBlockN;
+          // Q tiles: after the previous item's last QK^T has read the buffers
+          ok = mbar_wait(bar_qempty, (k & 1) ^ 1);
           if (!ok) break;
-          mbar_arrive_expect_tx(bar_vfull(v), C::kTileBytes);
-          for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(smem_u32(sV + v * C::kTileBytes + b * C::kBoxBytes), &tmap_v, b * 64, head,
-                        row, bar_vfull(v));
-          issued_v = j + 1;
+          for (int t = 0; t < (has1 ? 2 : 1); ++t) {
+            mbar_arrive_expect_tx(bar_qfull(t), C::kTileBytes);
+            for (int b = 0; b < C::kBoxes; ++b)
+              tma_load_3d(smem_u32(sQ + t * C::kTileBytes + b * C::kBoxBytes), &tmap_q, b * 64,
+                          d.head, d.q0 + t * kBlockM, bar_qfull(t));
+            ++qn[t];
+          }
+          for (int j = 0; j < nkv && ok; ++j) {
+            const int row = d.seg_start + j * kBlockN;
+            const int s = static_cast<int>(kt % SK);
+            ok = mbar_wait(bar_kempty(s), ((kt / SK) & 1) ^ 1);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar_kfull(s), C::kTileBytes);
+            for (int b = 0; b < C::kBoxes; ++b)
+              tma_load_3d(smem_u32(sK + s * C::kTileBytes + b * C::kBoxBytes), &tmap_k, b * 64,
+                          d.head, row, bar_kfull(s));
+            ++kt;
+            const int v = static_cast<int>(vt % SV);
+            ok = mbar_wait(bar_vempty(v), ((vt / SV) & 1) ^ 1);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar_vfull(v), C::kTileBytes);
+            for (int b = 0; b < C::kBoxes; ++b)
+              tma_load_3d(smem_u32(sV + v * C::kTileBytes + b * C::kBoxBytes), &tmap_v, b * 64,
+                          d.head, row, bar_vfull(v));
+            ++vt;
+          }
         }
         if (!ok) record_error(err, kErrTimeout);
         // Drain: never leave the CTA while a bulk copy may still be landing in shared memory.
-        // The last S loads of each kind sit on distinct stages, so each stage's latest phase is
+        // The last loads of each ring sit on distinct stages, so each stage's latest phase is
         // the one to wait for (already complete in the normal path).
-        for (int t = 0; t < (has1 ? 2 : 1); ++t) mbar_wait(bar_qfull(t), 0);
-        for (int j = issued_k - 1; j >= 0 && j >= issued_k - SK; --j)
-          mbar_wait(bar_kfull(j % SK), (j / SK) & 1);
-        for (int j = issued_v - 1; j >= 0 && j >= issued_v - SV; --j)
-          mbar_wait(bar_vfull(j % SV), (j / SV) & 1);
+        for (int t = 0; t < 2; ++t)
+          if (qn[t] > 0) mbar_wait(bar_qfull(t), (qn[t] - 1) & 1);
+        for (uint32_t i = 0; i < SK && i < kt; ++i) {
+          const uint32_t x = kt - 1 - i;
+          mbar_wait(bar_kfull(x % SK), (x / SK) & 1);
+        }
+        for (uint32_t i = 0; i < SV && i < vt; ++i) {
+          const uint32_t x = vt - 1 - i;
+          mbar_wait(bar_vfull(x % SV), (x / SV) & 1);
+        }
       }
     } else if (warp == 9) {
       // ================= MMA issuer =================
@@ -204,98 +347,128 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       auto wait_all = [&](uint32_t bar, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(bar, parity));
       };
-      const uint32_t qa0 = smem_u32(sQ);
+      // Shared-memory descriptors are built once; each MMA adds a compile-time offset (in
+      // 16-byte units) to the low half, keeping the single issuing thread's work per MMA small.
+      const SmemDesc dq = sw128_desc_split(smem_u32(sQ), 16, 1024);
+      const SmemDesc dk = sw128_desc_split(smem_u32(sK), 16, 1024);
+      const SmemDesc dv = sw128_desc_split(smem_u32(sV), C::kBoxBytes, 1024);
+      constexpr uint32_t kTile16 = C::kTileBytes >> 4;
       auto issue_qk = [&](int t, int s) {  // S_t = Q_t K_s^T
         const uint32_t d = tmem + kColS + 128 * t;
-        const uint32_t qa = qa0 + t * C::kTileBytes;
-        const uint32_t kb = smem_u32(sK + s * C::kTileBytes);
+        const uint32_t qlo = dq.lo + t * kTile16;
+        const uint32_t klo = dk.lo + s * kTile16;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          mma_ss(d, sw128_desc(qa + off, 16, 1024), sw128_desc(kb + off, 16, 1024), C::kIdescQK,
-                 kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss_split(d, qlo + off, dq.hi, klo + off, dk.hi, C::kIdescQK, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar_sfull(t));
       };
       auto issue_pv = [&](int t, int s, bool first) {  // O_t += P_t V_s
         const uint32_t p = tmem + kColS + 128 * t;
-        const uint32_t vb = smem_u32(sV + s * C::kTileBytes);
+        const uint32_t vlo = dv.lo + s * kTile16;
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
           // 16 keys per MMA: 8 TMEM columns of packed bf16 P; 16 rows (2 KB) of V
-          mma_ts(tmem + kColO + 128 * t, p + kk * 8, sw128_desc(vb + kk * 2048, C::kBoxBytes, 1024),
-                 C::kIdescPV, (!first || kk > 0) ? 1u : 0u);
+          mma_ts_split(tmem + kColO + 128 * t, p + kk * 8, vlo + kk * (2048 >> 4), dv.hi,
+                       C::kIdescPV, (!first || kk > 0) ? 1u : 0u);
       };
+      const bool leader = elect_one();  // the one thread that issues MMAs and commits
 
-      bool ok = wait_all(bar_qfull(0), 0);
-      if (ok && has1) ok = wait_all(bar_qfull(1), 0);
-      if (ok) ok = wait_all(bar_kfull(0), 0);
-      if (ok) {
-        tc_fence_after();
-        if (lane == 0) {
-          issue_qk(0, 0);
-          if (has1) issue_qk(1, 0);
-          mma_commit(bar_kempty(0));
-        }
+      uint32_t kc = 0, vc = 0;                  // K / V tiles consumed so far
+      uint32_t qn[2] = {0u, 0u}, pn[2] = {0u, 0u}, un[2] = {0u, 0u};  // per query tile slot
+      bool ok = true, issued = false;
+      for (int k = 0; ok; ++k) {
+        ok = wait_all(bar_wfull(k & 1), (k >> 1) & 1);
+        if (!ok) break;
+        const WorkDesc d = work[k & 1];
         __syncwarp();
-      }
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int sv = j % SV;
-        const bool more = j + 1 < nkv;
-        const int sk = (j + 1) % SK;
-        ok = wait_all(bar_vfull(sv), (j / SV) & 1);
-        if (!ok) break;
-        if (j == nkv - 1 && kv_last_valid < kBlockN) {
-          // Zero the value rows past the segment end (rows are 128 B per box; the swizzle only
-          // permutes 16-byte chunks within a row, so whole rows are cleared wherever they sit).
-          uint8_t* vb = sV + sv * C::kTileBytes;
-          const int nrows = kBlockN - kv_last_valid;
-          for (int idx = lane; idx < nrows * C::kBoxes * 8; idx += 32) {
-            const int r = kv_last_valid + idx / (C::kBoxes * 8);
-            const int rem = idx % (C::kBoxes * 8);
-            *reinterpret_cast<uint4*>(vb + (rem >> 3) * C::kBoxBytes + r * 128 + (rem & 7) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        // tile 0: PV0_j, then S0_{j+1}
-        ok = wait_all(bar_pfull(0), j & 1);
-        if (!ok) break;
-        if (more) ok = wait_all(bar_kfull(sk), ((j + 1) / SK) & 1);
+        if (leader) mbar_arrive(bar_wempty(k & 1));
+        if (d.seg_len < 0) break;
+        const int seg_end = d.seg_start + d.seg_len;
+        const bool has1 = d.q0 + kBlockM < seg_end;
+        const int nkv = (d.seg_len + kBlockN - 1) / kBlockN;
+        const int kv_last_valid = d.seg_len - (nkv - 1) * kBlockN;  // keys in the last tile
+
+        ok = wait_all(bar_qfull(0), qn[0]++ & 1);
+        if (ok && has1) ok = wait_all(bar_qfull(1), qn[1]++ & 1);
+        if (ok) ok = wait_all(bar_kfull(kc % SK), (kc / SK) & 1);
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
-          issue_pv(0, sv, j == 0);
-          if (!more) mma_commit(bar_ofinal(0));
-          if (more) issue_qk(0, sk);
-          if (!has1) {
-            mma_commit(bar_vempty(sv));
-            if (more) mma_commit(bar_kempty(sk));
-          }
+        if (leader) {
+          issue_qk(0, kc % SK);
+          if (has1) issue_qk(1, kc % SK);
+          if (nkv == 1) mma_commit(bar_qempty);  // the item's last QK^T: Q may be reloaded
+          mma_commit(bar_kempty(kc % SK));
         }
+        issued = true;
         __syncwarp();
-        if (has1) {
-          // tile 1: PV1_j, then S1_{j+1}
-          ok = wait_all(bar_pfull(1), j & 1);
+        ++kc;
+        for (int j = 0; j < nkv && ok; ++j) {
+          const int sv = static_cast<int>(vc % SV);
+          const bool more = j + 1 < nkv;
+          const int sk = static_cast<int>(kc % SK);
+          ok = wait_all(bar_vfull(sv), (vc / SV) & 1);
+          if (!ok) break;
+          if (j == nkv - 1 && kv_last_valid < kBlockN) {
+            // Zero the value rows past the segment end (rows are 128 B per box; the swizzle only
+            // permutes 16-byte chunks within a row, so whole rows are cleared wherever they sit).
+            uint8_t* vb = sV + sv * C::kTileBytes;
+            const int nrows = kBlockN - kv_last_valid;
+            for (int idx = lane; idx < nrows * C::kBoxes * 8; idx += 32) {
+              const int r = kv_last_valid + idx / (C::kBoxes * 8);
+              const int rem = idx % (C::kBoxes * 8);
+              *reinterpret_cast<uint4*>(vb + (rem >> 3) * C::kBoxBytes + r * 128 + (rem & 7) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          // tile 0: PV0_j (the item's first one waits for the previous epilogue), then S0_{j+1}
+          ok = wait_all(bar_pfull(0), pn[0]++ & 1);
+          if (ok && j == 0) ok = wait_all(bar_oempty(0), (un[0] & 1) ^ 1);
+          if (ok && more) ok = wait_all(bar_kfull(sk), (kc / SK) & 1);
           if (!ok) break;
           tc_fence_after();
-          if (lane == 0) {
-            issue_pv(1, sv, j == 0);
-            mma_commit(bar_vempty(sv));
-            if (!more) mma_commit(bar_ofinal(1));
-            if (more) {
-              issue_qk(1, sk);
-              mma_commit(bar_kempty(sk));
+          if (leader) {
+            issue_pv(0, sv, j == 0);
+            if (!more) mma_commit(bar_ofinal(0));
+            if (more) issue_qk(0, sk);
+            if (!has1) {
+              mma_commit(bar_vempty(sv));
+              if (more) mma_commit(bar_kempty(sk));
+              if (j + 2 == nkv) mma_commit(bar_qempty);
             }
           }
           __syncwarp();
+          if (has1) {
+            // tile 1: PV1_j, then S1_{j+1}
+            ok = wait_all(bar_pfull(1), pn[1]++ & 1);
+            if (ok && j == 0) ok = wait_all(bar_oempty(1), (un[1] & 1) ^ 1);
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) {
+              issue_pv(1, sv, j == 0);
+              mma_commit(bar_vempty(sv));
+              if (!more) mma_commit(bar_ofinal(1));
+              if (more) {
+                issue_qk(1, sk);
+                mma_commit(bar_kempty(sk));
+                if (j + 2 == nkv) mma_commit(bar_qempty);
+              }
+            }
+            __syncwarp();
+          }
+          ++vc;
+          if (more) ++kc;
         }
+        ++un[0];
+        if (has1) ++un[1];
       }
-      if (!ok && lane == 0) record_error(err, kErrTimeout);
+      if (!ok && leader) record_error(err, kErrTimeout);
       // Drain: the commit arrives once every MMA issued above has completed, so TMEM is idle
       // before it is released (the normal path has already waited for the last PV).
-      if (lane == 0) {
+      if (issued && leader) {
         mma_commit(bar_drain);
         mbar_wait(bar_drain, 0);
       }
@@ -303,19 +476,31 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     }
   } else {
     setmaxnreg_inc<kRegsSoftmax>();
-    if (warp < 4 || has1) {
-      // ============ softmax / correction / epilogue (warps 0-3: tile 0, 4-7: tile 1) ============
-      const int t = warp >> 2;
-      const int row = threadIdx.x & 127;  // query row within the tile == TMEM lane
-      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-      const uint32_t s_addr = tmem + lane_base + kColS + 128 * t;
-      const uint32_t o_addr = tmem + lane_base + kColO + 128 * t;
-      const float2 c2 = make_float2(scale_log2, scale_log2);
+    // ============ softmax / correction / epilogue (warps 0-3: tile 0, 4-7: tile 1) ============
+    const int t = warp >> 2;
+    const int row = threadIdx.x & 127;  // query row within the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + kColS + 128 * t;
+    const uint32_t o_addr = tmem + lane_base + kColO + 128 * t;
+    const float2 c2 = make_float2(scale_log2, scale_log2);
+    uint32_t sn = 0, fn = 0;  // S groups and final-O completions seen by this tile slot
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_wfull(k & 1), (k >> 1) & 1));
+      if (!ok) break;
+      const WorkDesc d = work[k & 1];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_wempty(k & 1));
+      if (d.seg_len < 0) break;
+      const int seg_end = d.seg_start + d.seg_len;
+      const bool has1 = d.q0 + kBlockM < seg_end;
+      if (t == 1 && !has1) continue;
+      const int nkv = (d.seg_len + kBlockN - 1) / kBlockN;
+      const int kv_last_valid = d.seg_len - (nkv - 1) * kBlockN;
       float m_used = -INFINITY;  // reference max (raw score units) used in the exponent
       float l = 0.f;
-      bool ok = true;
       for (int j = 0; j < nkv; ++j) {
-        ok = mbar_wait(bar_sfull(t), j & 1);
+        ok = mbar_wait(bar_sfull(t), sn++ & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         uint32_t sr[128];
@@ -384,41 +569,39 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         tc_fence_before();
         mbar_arrive(bar_pfull(t));
       }
-      // ---- epilogue: O / l -> bf16 rows of this segment; LSE ----
-      if (ok) {
-        ok = mbar_wait(bar_ofinal(t), 0);
-        ok = __all_sync(0xffffffffu, ok);
-      }
-      if (ok) {
-        tc_fence_after();
-        const int q_row = q0 + t * kBlockM + row;
-        const bool valid = q_row < seg_end;
-        const float inv_l = 1.f / l;
-        __nv_bfloat16* orow = out + (static_cast<size_t>(q_row) * num_heads + head) * D;
+      if (!ok) break;
+      // ---- epilogue: O / l -> bf16 rows of this segment; LSE; then O_t is free again ----
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_ofinal(t), fn++ & 1));
+      if (!ok) break;
+      tc_fence_after();
+      const int q_row = d.q0 + t * kBlockM + row;
+      const bool valid = q_row < seg_end;
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* orow = out + (static_cast<size_t>(q_row) * num_heads + d.head) * D;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t orr[32];
-          tmem_ld32(o_addr + c0, orr);
-          tmem_ld_wait();
-          tmem_reg_fence<32>(orr);
-          uint32_t pk[16];
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t orr[32];
+        tmem_ld32(o_addr + c0, orr);
+        tmem_ld_wait();
+        tmem_reg_fence<32>(orr);
+        uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            pk[c] = pack_bf16x2(__uint_as_float(orr[2 * c]) * inv_l,
-                                __uint_as_float(orr[2 * c + 1]) * inv_l);
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+        for (int c = 0; c < 16; ++c)
+          pk[c] = pack_bf16x2(__uint_as_float(orr[2 * c]) * inv_l,
+                              __uint_as_float(orr[2 * c + 1]) * inv_l);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-          }
+          for (int c = 0; c < 4; ++c)
+            dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         }
-        if (lse != nullptr && valid)
-          lse[static_cast<size_t>(head) * capacity + q_row] = m_used * scale + logf(l);
-      } else if (lane == 0) {
-        record_error(err, kErrTimeout);
       }
+      tc_fence_before();
+      mbar_arrive(bar_oempty(t));
+      if (lse != nullptr && valid)
+        lse[static_cast<size_t>(d.head) * capacity + q_row] = m_used * scale + logf(l);
     }
+    if (!ok && lane == 0) record_error(err, kErrTimeout);
   }
 
   // ---- teardown: every MMA has completed (drained above), then release TMEM ----
@@ -428,6 +611,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+int num_sms_of_current_device() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
 }
 
 template <int D>
@@ -444,16 +639,33 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int qtiles = (a.max_seqlen + kBlockM - 1) / kBlockM;
-  const dim3 grid((qtiles + kTilesPerCta - 1) / kTilesPerCta, a.num_heads, a.num_segments);
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  uint32_t* ws = static_cast<uint32_t*>(a.workspace);
+  attn_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.cu_seqlens, a.num_segments, a.capacity,
+                                                   a.max_seqlen, a.num_heads, ws, a.err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // short segments: one CTA per SM (one fits per SM by shared memory and TMEM) looping over
+  // items; long segments: one CTA per item.  Never more CTAs than the largest possible number
+  // of items (CTAs past the actual count leave at once).
+  const long long max_items =
+      (static_cast<long long>(a.capacity) / kRowsPerItem + a.num_segments) * a.num_heads;
+  const long long want = a.max_seqlen <= kPersistMaxSeqlen ? sms : max_items;
+  const int grid = static_cast<int>(max_items < want ? max_items : want);
   const float scale_log2 = a.scale * 1.4426950408889634f;
   attn_fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(
       a.tmap_q, a.tmap_k, a.tmap_v, static_cast<__nv_bfloat16*>(a.o), a.lse, a.cu_seqlens,
-      a.capacity, a.num_heads, a.scale, scale_log2, a.err);
+      a.num_segments, a.capacity, a.num_heads, a.scale, scale_log2, ws, a.err);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+size_t attn_workspace_bytes(int num_segments) {
+  const size_t bytes = workspace_words(num_segments) * sizeof(uint32_t);
+  return (bytes + 255) / 256 * 256;
+}
 
 cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t stream) {
   if (a.max_seqlen <= 0 || a.num_segments <= 0) return cudaSuccess;

@@ -59,9 +59,11 @@ struct AttnArgs {
   int num_heads;
   int head_dim;
   float scale;
+  void* workspace;  // attn_workspace_bytes(num_segments) bytes: the work plan
   unsigned int* err;
 };
 
+size_t attn_workspace_bytes(int num_segments);
 cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t stream);
 
 }  // namespace h3

@@ -174,11 +174,11 @@ h3_status h3_rope_apply(const void* q_in, void* q_out, const void* k_in, void* k
 
 size_t h3_varlen_attn_workspace_size(int32_t num_segments, int32_t num_heads, int32_t max_seqlen,
                                      int32_t head_dim) {
-  (void)num_segments;
   (void)num_heads;
   (void)max_seqlen;
   (void)head_dim;
-  return 0;
+  if (num_segments <= 0) return 0;
+  return h3::attn_workspace_bytes(num_segments);
 }
 
 h3_status h3_varlen_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -199,6 +199,10 @@ h3_status h3_varlen_attn_fwd(const void* q, const void* k, const void* v, void* 
     return H3_ERR_MISALIGNED;
   const size_t need = h3_varlen_attn_workspace_size(num_segments, num_heads, max_seqlen, head_dim);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return H3_ERR_WORKSPACE;
+  if (workspace != nullptr && !aligned16(workspace)) return H3_ERR_MISALIGNED;
+  // work items are counted in 32 bits: (capacity / 256 + segments) * heads must fit
+  if ((static_cast<int64_t>(capacity) / 256 + num_segments) * num_heads > INT32_MAX)
+    return H3_ERR_INVALID_ARG;
   if (num_segments == 0 || max_seqlen == 0 || capacity == 0) return H3_OK;
   if (!device_is_sm103()) return H3_ERR_UNSUPPORTED;
 
@@ -216,6 +220,7 @@ h3_status h3_varlen_attn_fwd(const void* q, const void* k, const void* v, void* 
   a.num_heads = num_heads;
   a.head_dim = head_dim;
   a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(head_dim));
+  a.workspace = workspace;
   a.err = device_error_ptr();
   if (a.err == nullptr) return H3_ERR_CUDA;
   return from_cuda(h3::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));

@@ -50,6 +50,12 @@ def test_library_exports_nothing_else():
     assert exported == _declared()
 
 
+def test_workspace_size_grows_with_segments(lib):
+    sizes = [lib.h3_varlen_attn_workspace_size(s, 40, 58000, 128) for s in (1, 3, 693, 65535)]
+    assert all(x % 256 == 0 for x in sizes) and sizes == sorted(sizes)
+    assert sizes[-1] >= 8 * 65535 and lib.h3_varlen_attn_workspace_size(0, 40, 1, 128) == 0
+
+
 def test_version_and_status_strings(lib):
     assert lib.h3_version() == 100
     for s in range(10):
@@ -81,18 +87,23 @@ FAKE = 0x1000  # never dereferenced: every call below is rejected by host-side v
 def test_attn_rejects_bad_arguments_on_the_host(lib):
     f = lib.h3_varlen_attn_fwd
     P = ctypes.c_void_p
-    ok = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, cu=FAKE, S=3, maxs=128, C=256, H=2, D=128)
+    need = lib.h3_varlen_attn_workspace_size(3, 2, 128, 128)
+    ok = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, cu=FAKE, S=3, maxs=128, C=256, H=2, D=128,
+              ws=FAKE, wsb=need)
 
     def call(**kw):
         a = dict(ok, **kw)
         return f(P(a["q"]), P(a["k"]), P(a["v"]), P(a["o"]), P(a["lse"]) if a["lse"] else None,
-                 P(a["cu"]) if a["cu"] else None, a["S"], a["maxs"], a["C"], a["H"], a["D"], 0.0, None, 0, None)
+                 P(a["cu"]) if a["cu"] else None, a["S"], a["maxs"], a["C"], a["H"], a["D"], 0.0,
+                 P(a["ws"]) if a["ws"] else None, a["wsb"], None)
 
     assert call(q=0) == 1 and call(cu=0) == 1 and call(o=0) == 1          # H3_ERR_NULL
     assert call(S=-1) == 2 and call(H=0) == 2 and call(maxs=512) == 2      # max_seqlen > capacity
     assert call(D=96) == 4                                                # H3_ERR_UNSUPPORTED
     assert call(q=FAKE + 8) == 8 and call(lse=FAKE + 2) == 8              # H3_ERR_MISALIGNED
-    assert call(S=0) == 0 and call(maxs=0) == 0                           # nothing to do
+    assert call(ws=0) == 5 and call(wsb=need - 1) == 5                    # H3_ERR_WORKSPACE
+    assert call(ws=FAKE + 4) == 8
+    assert call(S=0, ws=0, wsb=0) == 0 and call(maxs=0) == 0              # nothing to do
 
 
 def test_rope_rejects_bad_arguments_on_the_host(lib):
