@@ -145,6 +145,32 @@ H3_API h3_status h3_varlen_attn_fwd(const void* q, const void* k, const void* v,
                              float softmax_scale, void* workspace, size_t workspace_bytes,
                              h3_stream_t stream);
 
+/* Largest num_segments h3_varlen_attn_fwd_noalloc accepts. */
+#define H3_NOALLOC_MAX_SEGMENTS 16384
+
+/* h3_varlen_attn_fwd without a workspace argument, for callers that cannot allocate device
+ * memory -- for example code running where a cudaMalloc would synchronise the device or is not
+ * permitted (inside a caller's own memory pool or allocator, a plugin host that owns all device
+ * memory, a latency-critical loop).  The pages have no counterpart: this is a convenience of the
+ * library, not a step of the method.
+ *
+ * Same inputs, outputs, semantics and errors as h3_varlen_attn_fwd.  Instead of a workspace it
+ * uses a fixed array inside the library (132 KB per device, held from the first use until the
+ * process exits), so it calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - At most H3_NOALLOC_MAX_SEGMENTS segments; more returns H3_ERR_WORKSPACE, launching nothing.
+ *   - The first call on each device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - All calls on a device share the array.  Calls whose kernels may overlap on the GPU (other
+ *     streams, other host threads) race on it and must not be issued; serialise them, or use
+ *     h3_varlen_attn_fwd with a workspace per stream.
+ *   - Each call rewrites every part of the array it reads, so nothing needs clearing between
+ *     calls. */
+H3_API h3_status h3_varlen_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o,
+                                            float* lse, const int32_t* cu_seqlens,
+                                            int32_t num_segments, int32_t max_seqlen,
+                                            int32_t capacity, int32_t num_heads, int32_t head_dim,
+                                            float softmax_scale, h3_stream_t stream);
+
 /* Number of windows of the partition (host only; no device work).
  * [H3-fast] "window attention across GPUs": along each axis of length L with window w and
  * shift s there are ceil((L + s) / w) windows (edge windows cropped).  Returns -1 on bad input

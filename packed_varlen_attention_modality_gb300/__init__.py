@@ -20,6 +20,7 @@ from typing import Optional, Sequence, Tuple
 import torch
 
 __all__ = ["H3Error", "RopeConfig", "lib_path", "load_library", "rope_apply", "varlen_attn_fwd",
+           "varlen_attn_fwd_noalloc",
            "varlen_attn_workspace_size", "window_count", "window_pack", "window_unpack",
            "get_device_error", "TAG_TEXT", "TAG_VIDEO", "TAG_AUDIO"]
 
@@ -71,6 +72,7 @@ def load_library():
                                 ctypes.POINTER(RopeConfig), P]),
         "h3_varlen_attn_workspace_size": (U64, [I32, I32, I32, I32]),
         "h3_varlen_attn_fwd": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, F32, P, U64, P]),
+        "h3_varlen_attn_fwd_noalloc": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, F32, P]),
         "h3_window_count": (I32, [I32P, I32P, I32P]),
         "h3_window_pack": (I32, [I32P, I32P, I32P, P, P, ctypes.POINTER(P), ctypes.POINTER(P),
                                  I32, I32, P]),
@@ -210,6 +212,37 @@ def varlen_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                                     _ptr(workspace), ws_bytes, _stream(dev))
     _check(st, "h3_varlen_attn_fwd")
     return (out, lse) if (return_lse or lse is not None) else out
+
+
+def varlen_attn_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                            cu_seqlens: torch.Tensor, max_seqlen: int, out: torch.Tensor,
+                            lse: Optional[torch.Tensor] = None,
+                            softmax_scale: Optional[float] = None) -> torch.Tensor:
+    """varlen_attn_fwd through the entry point that allocates no device memory.
+
+    For callers that cannot allocate: `out` (and `lse`, if wanted) must be given, and the
+    library uses its own fixed scratch array (at most 16384 segments).  Calls on one device must
+    not overlap on the GPU; the first call on a device should come before any stream capture.
+    """
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _require(t, name, torch.bfloat16, dev)
+    if q.dim() != 3 or k.shape != q.shape or v.shape != q.shape or out.shape != q.shape:
+        raise ValueError("q, k, v, out must all be [C, H, D]")
+    C, H, D = q.shape
+    _require(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    if lse is not None:
+        _require(lse, "lse", torch.float32, dev)
+        if tuple(lse.shape) != (H, C):
+            raise ValueError("lse must be [H, C]")
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        st = lib.h3_varlen_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                            _ptr(cu_seqlens), cu_seqlens.numel() - 1,
+                                            int(max_seqlen), C, H, D, scale, _stream(dev))
+    _check(st, "h3_varlen_attn_fwd_noalloc")
+    return out
 
 
 def window_count(grid: Sequence[int], win: Sequence[int], shift: Sequence[int]) -> int:

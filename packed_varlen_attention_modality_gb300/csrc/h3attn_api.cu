@@ -14,6 +14,13 @@
 #include "h3attn.h"
 #include "h3_internal.h"
 
+// Scratch for h3_varlen_attn_fwd_noalloc: the attention work plan lives in this fixed array
+// instead of a caller-provided workspace.  Every device that loads the library holds it (132 KB,
+// enough for H3_NOALLOC_MAX_SEGMENTS segments) until the process exits.  It is shared by all
+// calls on a device.
+constexpr int kNoallocScratchBytes = 132 * 1024;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
 namespace {
 
 __device__ unsigned int g_device_error;
@@ -84,6 +91,23 @@ bool device_is_sm103() {
 }
 
 h3_status from_cuda(cudaError_t e) { return e == cudaSuccess ? H3_OK : H3_ERR_CUDA; }
+
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device.  The name of a __device__ array in
+// host code is only a host-side stand-in, so the real address is looked up once per device with
+// that device current; nullptr on failure.
+void* noalloc_scratch_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    g_noalloc_ptr[dev] = p;
+  }
+  return g_noalloc_ptr[dev];
+}
 
 }  // namespace
 
@@ -221,6 +245,52 @@ h3_status h3_varlen_attn_fwd(const void* q, const void* k, const void* v, void* 
   a.head_dim = head_dim;
   a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(head_dim));
   a.workspace = workspace;
+  a.err = device_error_ptr();
+  if (a.err == nullptr) return H3_ERR_CUDA;
+  return from_cuda(h3::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+h3_status h3_varlen_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o,
+                                     float* lse, const int32_t* cu_seqlens, int32_t num_segments,
+                                     int32_t max_seqlen, int32_t capacity, int32_t num_heads,
+                                     int32_t head_dim, float softmax_scale, h3_stream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || cu_seqlens == nullptr)
+    return H3_ERR_NULL;
+  if (num_segments < 0 || num_segments > 65535 || max_seqlen < 0 || capacity < 0 ||
+      num_heads <= 0 || num_heads > 65535)
+    return H3_ERR_INVALID_ARG;
+  if (max_seqlen > capacity) return H3_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return H3_ERR_UNSUPPORTED;
+  if (!(softmax_scale <= 0.f || std::isfinite(softmax_scale))) return H3_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return H3_ERR_MISALIGNED;
+  // the plan must fit the fixed array: refuse more segments than it was sized for
+  if (num_segments > H3_NOALLOC_MAX_SEGMENTS ||
+      h3::attn_workspace_bytes(num_segments) > static_cast<size_t>(kNoallocScratchBytes))
+    return H3_ERR_WORKSPACE;
+  if ((static_cast<int64_t>(capacity) / 256 + num_segments) * num_heads > INT32_MAX)
+    return H3_ERR_INVALID_ARG;
+  if (num_segments == 0 || max_seqlen == 0 || capacity == 0) return H3_OK;
+  if (!device_is_sm103()) return H3_ERR_UNSUPPORTED;
+
+  void* scratch = noalloc_scratch_ptr();
+  if (scratch == nullptr) return H3_ERR_CUDA;
+  h3::AttnArgs a{};
+  if (!make_qkv_map(&a.tmap_q, q, capacity, num_heads, head_dim) ||
+      !make_qkv_map(&a.tmap_k, k, capacity, num_heads, head_dim) ||
+      !make_qkv_map(&a.tmap_v, v, capacity, num_heads, head_dim))
+    return H3_ERR_CUDA;
+  a.o = o;
+  a.lse = lse;
+  a.cu_seqlens = cu_seqlens;
+  a.num_segments = num_segments;
+  a.max_seqlen = max_seqlen;
+  a.capacity = capacity;
+  a.num_heads = num_heads;
+  a.head_dim = head_dim;
+  a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(head_dim));
+  a.workspace = scratch;  // the plan kernel rewrites every word the attention kernel reads
   a.err = device_error_ptr();
   if (a.err == nullptr) return H3_ERR_CUDA;
   return from_cuda(h3::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
