@@ -60,6 +60,23 @@ def load_peaks():
 
 
 # ------------------------------------------------------------------------------------------------
+# replicas: every rank runs the same workload (weak scaling); the job time is the slowest rank's
+# ------------------------------------------------------------------------------------------------
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """Slowest rank's time (no-op for one rank); works on any process-group backend."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(work_per_rank: float, world: int, job_ms: float) -> float:
+    """Whole-job TFLOP/s: the work of all replicas over the slowest replica's time."""
+    return world * work_per_rank / (job_ms / 1e3) / 1e12
+
+
+# ------------------------------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ------------------------------------------------------------------------------------------------
 class ClockSampler:
@@ -260,17 +277,13 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
-    total_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     if h3.get_device_error(dev) != 0:
         raise RuntimeError("device error during the timed steps")
     rope_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     attn_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
     ms_per_step = total_ms / args.steps
-    value = world * flops / (ms_per_step / 1e3) / 1e12
+    value = job_throughput(flops, world, ms_per_step)
 
     attn_tflops = flops / (attn_ms / 1e3) / 1e12
     rope_bytes = 4.0 * N * H * D * 2 + 13.0 * N  # read+write Q and K (bf16) + pos (12 B) + tag (1 B)
@@ -315,12 +328,8 @@ def run_ours(args, rank, world, local_rank):
             e2e_step()
         s1.record(stream)
         torch.cuda.synchronize(dev)
-        e_ms = s0.elapsed_time(s1) / n_e2e
-        if world > 1:
-            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * flops / (e_ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(bi),
+        e_ms = max_over_ranks(s0.elapsed_time(s1) / n_e2e, world, dev)
+        e2e = {"value": job_throughput(flops, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": int(bi),
                "d2h_bytes_per_step": int(bo), "ms_per_step": e_ms}
         del host, o_host, dq, dk, dv
 
