@@ -198,6 +198,28 @@ H3_API h3_status h3_window_pack(const int32_t grid[3], const int32_t win[3], con
                          const void* const* src, void* const* dst, int32_t num_tensors,
                          int32_t row_bytes, h3_stream_t stream);
 
+/* Shifted 3D window attention computed in place on the grid: the same result as
+ * h3_window_pack -> h3_varlen_attn_fwd over the window segments -> h3_window_unpack, without the
+ * packed copies.
+ *
+ * [H3-fast] "window attention across GPUs": every window of the (T, H, W) grid (windows win,
+ * shifted by shift, edge windows cropped) attends within itself; the output stays in the
+ * original token order.  Each window's rows are read straight from the grid with 5-D tensor
+ * loads (a 128-row tile = whole frames of one window); rows of an edge window's box that fall
+ * outside the grid are never used as keys and never written.
+ *
+ * q, k, v, o : device bf16 [T*H*W, num_heads, head_dim], rows in row-major (t, h, w) order.
+ * lse        : device fp32 [num_heads, T*H*W] (natural log) or NULL.
+ * grid, win, shift : host int32[3] each; as for h3_window_pack.  Supported windows: win[1]*win[2]
+ *              divides 128 and win[0]*win[1]*win[2] <= 256 (e.g. 4x8x8); else H3_ERR_UNSUPPORTED.
+ * softmax_scale: <= 0 selects 1/sqrt(head_dim).  No workspace.
+ * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG, H3_ERR_UNSUPPORTED, H3_ERR_MISALIGNED, H3_ERR_CUDA.
+ */
+H3_API h3_status h3_window_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                                    const int32_t grid[3], const int32_t win[3],
+                                    const int32_t shift[3], int32_t num_heads, int32_t head_dim,
+                                    float softmax_scale, h3_stream_t stream);
+
 /* Restore original token order: dst row perm[j] = src row j, for j in [0, num_tokens).
  * [H3-fast] "window attention across GPUs" (token order restored after attention).
  * perm is device int32 [num_tokens] (a permutation of [0, num_tokens); an entry out of range is

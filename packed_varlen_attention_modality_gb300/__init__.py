@@ -9,6 +9,7 @@ Calls:
   rope_apply        modality-tagged RoPE of Q and K with the continuation time shift
   varlen_attn_fwd   block-diagonal softmax attention over cu_seqlens segments
   window_count / window_pack / window_unpack   shifted 3D window partition and row gather/scatter
+  window_attn_fwd   shifted 3D window attention read and written in place on the grid
   get_device_error  read (and clear) the device-side error word
 """
 from __future__ import annotations
@@ -20,7 +21,7 @@ from typing import Optional, Sequence, Tuple
 import torch
 
 __all__ = ["H3Error", "RopeConfig", "lib_path", "load_library", "rope_apply", "varlen_attn_fwd",
-           "varlen_attn_fwd_noalloc",
+           "varlen_attn_fwd_noalloc", "window_attn_fwd",
            "varlen_attn_workspace_size", "window_count", "window_pack", "window_unpack",
            "get_device_error", "TAG_TEXT", "TAG_VIDEO", "TAG_AUDIO"]
 
@@ -73,6 +74,7 @@ def load_library():
         "h3_varlen_attn_workspace_size": (U64, [I32, I32, I32, I32]),
         "h3_varlen_attn_fwd": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, F32, P, U64, P]),
         "h3_varlen_attn_fwd_noalloc": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, F32, P]),
+        "h3_window_attn_fwd": (I32, [P, P, P, P, P, I32P, I32P, I32P, I32, I32, F32, P]),
         "h3_window_count": (I32, [I32P, I32P, I32P]),
         "h3_window_pack": (I32, [I32P, I32P, I32P, P, P, ctypes.POINTER(P), ctypes.POINTER(P),
                                  I32, I32, P]),
@@ -243,6 +245,41 @@ def varlen_attn_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                             int(max_seqlen), C, H, D, scale, _stream(dev))
     _check(st, "h3_varlen_attn_fwd_noalloc")
     return out
+
+
+def window_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grid: Sequence[int],
+                    win: Sequence[int], shift: Sequence[int], out: Optional[torch.Tensor] = None,
+                    return_lse: bool = False, lse: Optional[torch.Tensor] = None,
+                    softmax_scale: Optional[float] = None):
+    """Shifted 3D window attention in place on the grid (no packed copies).
+
+    q, k, v: bf16 [T*H*W, heads, D] in row-major (t, h, w) token order.  Returns out (and lse
+    fp32 [heads, T*H*W] when requested), in the same order.
+    """
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name, torch.bfloat16, dev)
+    n = int(grid[0]) * int(grid[1]) * int(grid[2])
+    if q.dim() != 3 or q.shape[0] != n or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must be [T*H*W, heads, D]")
+    _, H, D = q.shape
+    out = torch.empty_like(q) if out is None else out
+    _require(out, "out", torch.bfloat16, dev)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if return_lse and lse is None:
+        lse = torch.empty((H, n), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _require(lse, "lse", torch.float32, dev)
+        if tuple(lse.shape) != (H, n):
+            raise ValueError("lse must be [heads, T*H*W]")
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        st = lib.h3_window_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _i3(grid),
+                                    _i3(win), _i3(shift), H, D, scale, _stream(dev))
+    _check(st, "h3_window_attn_fwd")
+    return (out, lse) if (return_lse or lse is not None) else out
 
 
 def window_count(grid: Sequence[int], win: Sequence[int], shift: Sequence[int]) -> int:

@@ -75,11 +75,89 @@ __host__ __device__ constexpr size_t workspace_words(int num_segments) {
 }
 
 struct WorkDesc {
-  int seg_start;
-  int seg_len;  // < 0: no more work
+  int seg_start;  // packed: first row of the segment
+  int seg_len;    // packed: rows of the segment; window: 1; < 0: no more work
   int head;
-  int q0;
+  int q0;         // packed: first query row of the item
+  int box[3];     // window: grid (t, h, w) of the first valid tile's box origin (may be < 0)
+  int ntiles;     // window: valid 128-row tiles of the window (1 or 2)
+  uint32_t mask[2][4];  // window: rows of each tile that lie inside the grid (= inside the window)
 };
+
+struct ItemShape {
+  bool has1;          // second query tile present
+  int nkv;            // key/value tiles
+  int kv_last_valid;  // keys in the last key tile (packed; 128 for windows, which use masks)
+};
+
+template <bool kWin>
+__device__ __forceinline__ ItemShape shape_of(const WorkDesc& d) {
+  if (kWin) return ItemShape{d.ntiles == 2, d.ntiles, kBlockN};
+  const int nkv = (d.seg_len + kBlockN - 1) / kBlockN;
+  return ItemShape{d.q0 + kBlockM < d.seg_start + d.seg_len, nkv, d.seg_len - (nkv - 1) * kBlockN};
+}
+
+// 128-bit row masks as (lo, hi) 64-bit halves.
+__device__ __forceinline__ void or_shifted(uint64_t& lo, uint64_t& hi, uint64_t lo_in, uint64_t hi_in,
+                                           int sh) {  // (lo, hi) |= (lo_in, hi_in) << sh, sh < 128
+  if (sh == 0) {
+    lo |= lo_in;
+    hi |= hi_in;
+  } else if (sh < 64) {
+    lo |= lo_in << sh;
+    hi |= (hi_in << sh) | (lo_in >> (64 - sh));
+  } else {
+    hi |= lo_in << (sh - 64);
+  }
+}
+__device__ __forceinline__ uint64_t low_bits(int n) {  // n in [0, 64]
+  return n >= 64 ? ~0ull : ((1ull << n) - 1ull);
+}
+
+// Window item -> descriptor.  Items are numbered window-major, head fastest, so CTAs working at
+// one time read neighbouring 256-byte pieces of the same token rows.  Along each axis the window's
+// box starts at i * w - s (the shifted grid; may be negative) and the rows inside the grid are
+// [max(0, start), min(L, start + w)): the rest of the box is zero-filled by TMA and masked.
+// The masks are built in registers: a frame mask (valid h rows x valid w run), then per tile the
+// valid frames of that tile.
+__device__ __forceinline__ WorkDesc decode_window(uint32_t item, const WindowAttnGeom& g,
+                                                  int num_heads) {
+  const int win = static_cast<int>(item / static_cast<uint32_t>(num_heads));
+  WorkDesc d{};
+  d.seg_len = 1;
+  d.head = static_cast<int>(item % static_cast<uint32_t>(num_heads));
+  const int iw = win % g.nwin[2], ih = (win / g.nwin[2]) % g.nwin[1], it = win / (g.nwin[2] * g.nwin[1]);
+  const int lo_t = it * g.w[0] - g.s[0], lo_h = ih * g.w[1] - g.s[1], lo_w = iw * g.w[2] - g.s[2];
+  const int vl_t = max(0, -lo_t), vh_t = min(g.w[0], g.L[0] - lo_t);
+  const int vl_h = max(0, -lo_h), vh_h = min(g.w[1], g.L[1] - lo_h);
+  const int vl_w = max(0, -lo_w), vh_w = min(g.w[2], g.L[2] - lo_w);
+  const int bt = g.frames_per_tile;
+  const int tile_lo = vl_t / bt, tile_hi = (vh_t + bt - 1) / bt;
+  d.ntiles = tile_hi - tile_lo;
+  d.box[0] = lo_t + tile_lo * bt;
+  d.box[1] = lo_h;
+  d.box[2] = lo_w;
+  // frame mask: bits fh * ww + fw for valid (fh, fw); ww <= 128 and pf = wh * ww <= 128
+  const int ww = g.w[2], pf = g.w[1] * g.w[2];
+  uint64_t flo = 0, fhi = 0;
+  const int run = vh_w - vl_w;
+  const uint64_t rlo = low_bits(min(run, 64)), rhi = run > 64 ? low_bits(run - 64) : 0ull;
+  for (int fh = vl_h; fh < vh_h; ++fh) or_shifted(flo, fhi, rlo, rhi, fh * ww + vl_w);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {  // ntiles <= 2: frames_per_tile * 2 covers the window's frames
+    if (k >= d.ntiles) break;
+    uint64_t tlo = 0, thi = 0;
+    for (int ft = 0; ft < bt; ++ft) {
+      const int t = (tile_lo + k) * bt + ft;  // box-local frame
+      if (t >= vl_t && t < vh_t) or_shifted(tlo, thi, flo, fhi, ft * pf);
+    }
+    d.mask[k][0] = static_cast<uint32_t>(tlo);
+    d.mask[k][1] = static_cast<uint32_t>(tlo >> 32);
+    d.mask[k][2] = static_cast<uint32_t>(thi);
+    d.mask[k][3] = static_cast<uint32_t>(thi >> 32);
+  }
+  return d;
+}
 
 __device__ __forceinline__ int checked_len(const int32_t* __restrict__ cu, int g, int capacity,
                                            int max_seqlen, unsigned int* err) {
@@ -185,19 +263,23 @@ struct Cfg {
   static constexpr int kNumBars = 3 + 2 * kStagesK + 2 * kStagesV + 12 + 1;
   static constexpr int kSmemBytes = 1024 /*alignment slack*/ +
                                     kTileBytes * (kTilesPerItem + kStagesK + kStagesV) +
-                                    kNumBars * 8 + 16 /*TMEM slot*/ + 2 * 16 /*work ring*/;
+                                    kNumBars * 8 + 16 /*TMEM slot*/ + 2 * sizeof(WorkDesc);
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(kBlockM, kBlockN, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, true);
 };
 
-template <int D>
+// kWin = false: packed varlen segments (cu_seqlens, 3-D tensor maps, rows of [capacity, H, D]).
+// kWin = true: windows of a (T, H, W) grid read in place (5-D tensor maps over [T, H, W, heads, D]
+// in row-major token order); the output goes back to the same positions.
+template <int D, bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, __nv_bfloat16* __restrict__ out,
                 float* __restrict__ lse, const int32_t* __restrict__ cu_seqlens, int num_segments,
                 int capacity, int num_heads, float scale, float scale_log2,
-                uint32_t* __restrict__ ws, unsigned int* err) {
+                uint32_t* __restrict__ ws, const __grid_constant__ WindowAttnGeom wg,
+                unsigned int* err) {
   using C = Cfg<D>;
   constexpr int SK = C::kStagesK;
   constexpr int SV = C::kStagesV;
@@ -273,7 +355,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     if (warp == 8) {
       // ================= scheduler + TMA producer =================
       if (lane == 0) {
-        const uint32_t total = ws[1];
+        const uint32_t total =
+            kWin ? static_cast<uint32_t>(wg.nwin[0] * wg.nwin[1] * wg.nwin[2] * num_heads) : ws[1];
         uint32_t kt = 0, vt = 0;  // K / V tiles loaded so far (positions in the rings)
         uint32_t qn[2] = {0u, 0u};  // Q tiles loaded so far, per tile slot
         bool ok = true;
@@ -281,7 +364,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           const uint32_t item = blockIdx.x + static_cast<uint32_t>(k) * gridDim.x;
           WorkDesc d;
           if (item < total) {
-            d = decode_item(item, ws, cu_seqlens, num_segments, num_heads);
+            d = kWin ? decode_window(item, wg, num_heads)
+                     : decode_item(item, ws, cu_seqlens, num_segments, num_heads);
           } else {
             d.seg_start = 0;
             d.seg_len = -1;
@@ -293,17 +377,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           work[k & 1] = d;
           mbar_arrive(bar_wfull(k & 1));
           if (d.seg_len < 0) break;
-          const int seg_end = d.seg_start + d.seg_len;
-          const bool has1 = d.q0 + kBlockM < seg_end;
-          const int nkv = (d.seg_len + kBlockN - 1) / kBlockN;
+          const ItemShape sh = shape_of<kWin>(d);
+          const bool has1 = sh.has1;
+          const int nkv = sh.nkv;
+          // tile loads: packed rows [row, row + 128) of one head; window box (w, h, t) of frames
+          auto load_tile = [&](uint8_t* dst, const CUtensorMap* map, int tile, int row,
+                               uint32_t bar) {
+            for (int b = 0; b < C::kBoxes; ++b) {
+              if constexpr (kWin)
+                tma_load_5d(smem_u32(dst + b * C::kBoxBytes), map, b * 64, d.head, d.box[2],
+                            d.box[1], d.box[0] + tile * wg.frames_per_tile, bar);
+              else
+                tma_load_3d(smem_u32(dst + b * C::kBoxBytes), map, b * 64, d.head, row, bar);
+            }
+          };
           // Q tiles: after the previous item's last QK^T has read the buffers
           ok = mbar_wait(bar_qempty, (k & 1) ^ 1);
           if (!ok) break;
           for (int t = 0; t < (has1 ? 2 : 1); ++t) {
             mbar_arrive_expect_tx(bar_qfull(t), C::kTileBytes);
-            for (int b = 0; b < C::kBoxes; ++b)
-              tma_load_3d(smem_u32(sQ + t * C::kTileBytes + b * C::kBoxBytes), &tmap_q, b * 64,
-                          d.head, d.q0 + t * kBlockM, bar_qfull(t));
+            load_tile(sQ + t * C::kTileBytes, &tmap_q, t, d.q0 + t * kBlockM, bar_qfull(t));
             ++qn[t];
           }
           for (int j = 0; j < nkv && ok; ++j) {
@@ -312,17 +405,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
             ok = mbar_wait(bar_kempty(s), ((kt / SK) & 1) ^ 1);
             if (!ok) break;
             mbar_arrive_expect_tx(bar_kfull(s), C::kTileBytes);
-            for (int b = 0; b < C::kBoxes; ++b)
-              tma_load_3d(smem_u32(sK + s * C::kTileBytes + b * C::kBoxBytes), &tmap_k, b * 64,
-                          d.head, row, bar_kfull(s));
+            load_tile(sK + s * C::kTileBytes, &tmap_k, j, row, bar_kfull(s));
             ++kt;
             const int v = static_cast<int>(vt % SV);
             ok = mbar_wait(bar_vempty(v), ((vt / SV) & 1) ^ 1);
             if (!ok) break;
             mbar_arrive_expect_tx(bar_vfull(v), C::kTileBytes);
-            for (int b = 0; b < C::kBoxes; ++b)
-              tma_load_3d(smem_u32(sV + v * C::kTileBytes + b * C::kBoxBytes), &tmap_v, b * 64,
-                          d.head, row, bar_vfull(v));
+            load_tile(sV + v * C::kTileBytes, &tmap_v, j, row, bar_vfull(v));
             ++vt;
           }
         }
@@ -385,10 +474,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         __syncwarp();
         if (leader) mbar_arrive(bar_wempty(k & 1));
         if (d.seg_len < 0) break;
-        const int seg_end = d.seg_start + d.seg_len;
-        const bool has1 = d.q0 + kBlockM < seg_end;
-        const int nkv = (d.seg_len + kBlockN - 1) / kBlockN;
-        const int kv_last_valid = d.seg_len - (nkv - 1) * kBlockN;  // keys in the last tile
+        const ItemShape sh = shape_of<kWin>(d);
+        const bool has1 = sh.has1;
+        const int nkv = sh.nkv;
+        const int kv_last_valid = sh.kv_last_valid;  // keys in the last tile (packed)
 
         ok = wait_all(bar_qfull(0), qn[0]++ & 1);
         if (ok && has1) ok = wait_all(bar_qfull(1), qn[1]++ & 1);
@@ -410,7 +499,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           const int sk = static_cast<int>(kc % SK);
           ok = wait_all(bar_vfull(sv), (vc / SV) & 1);
           if (!ok) break;
-          if (j == nkv - 1 && kv_last_valid < kBlockN) {
+          if (!kWin && j == nkv - 1 && kv_last_valid < kBlockN) {
             // Zero the value rows past the segment end (rows are 128 B per box; the swizzle only
             // permutes 16-byte chunks within a row, so whole rows are cleared wherever they sit).
             uint8_t* vb = sV + sv * C::kTileBytes;
@@ -493,10 +582,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       if (lane == 0) mbar_arrive(bar_wempty(k & 1));
       if (d.seg_len < 0) break;
       const int seg_end = d.seg_start + d.seg_len;
-      const bool has1 = d.q0 + kBlockM < seg_end;
+      const ItemShape sh = shape_of<kWin>(d);
+      const bool has1 = sh.has1;
       if (t == 1 && !has1) continue;
-      const int nkv = (d.seg_len + kBlockN - 1) / kBlockN;
-      const int kv_last_valid = d.seg_len - (nkv - 1) * kBlockN;
+      const int nkv = sh.nkv;
+      const int kv_last_valid = sh.kv_last_valid;
+      // window: which keys of each tile (and which of this tile's query rows) are in the grid
+      uint32_t wm0[4], wm1[4];
+      if constexpr (kWin) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          wm0[i] = d.mask[0][i];
+          wm1[i] = d.mask[1][i];
+        }
+      }
       float m_used = -INFINITY;  // reference max (raw score units) used in the exponent
       float l = 0.f;
       for (int j = 0; j < nkv; ++j) {
@@ -513,7 +612,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
-        if (j == nkv - 1 && kv_last_valid < kBlockN) {
+        if constexpr (kWin) {
+          // keys outside the grid (zero-filled rows of an edge window's box): -inf by select
+          uint32_t km[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) km[i] = j == 0 ? wm0[i] : wm1[i];
+          if ((km[0] & km[1] & km[2] & km[3]) != 0xffffffffu) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) s[c] = ((km[c >> 5] >> (c & 31)) & 1u) ? s[c] : -INFINITY;
+          }
+        } else if (j == nkv - 1 && kv_last_valid < kBlockN) {
           // keys past the segment end: -inf by select, so a NaN/Inf score there is discarded
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (c < kv_last_valid) ? s[c] : -INFINITY;
@@ -574,8 +682,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       ok = __all_sync(0xffffffffu, mbar_wait(bar_ofinal(t), fn++ & 1));
       if (!ok) break;
       tc_fence_after();
-      const int q_row = d.q0 + t * kBlockM + row;
-      const bool valid = q_row < seg_end;
+      int q_row;  // this thread's row in the output (original row-major order for windows)
+      bool valid;
+      if constexpr (kWin) {
+        const int pf = wg.w[1] * wg.w[2];
+        const int gt = d.box[0] + t * wg.frames_per_tile + row / pf;
+        const int gh = d.box[1] + (row / wg.w[2]) % wg.w[1];
+        const int gw = d.box[2] + row % wg.w[2];
+        uint32_t word = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if ((row >> 5) == i) word = t == 0 ? wm0[i] : wm1[i];
+        valid = (word >> (row & 31)) & 1u;
+        q_row = (gt * wg.L[1] + gh) * wg.L[2] + gw;
+      } else {
+        q_row = d.q0 + t * kBlockM + row;
+        valid = q_row < seg_end;
+      }
       const float inv_l = 1.f / l;
       __nv_bfloat16* orow = out + (static_cast<size_t>(q_row) * num_heads + d.head) * D;
 #pragma unroll 1
@@ -625,7 +748,7 @@ int num_sms_of_current_device() {
   return cached[dev];
 }
 
-template <int D>
+template <int D, bool kWin>
 cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
   using C = Cfg<D>;
   static bool configured[64] = {};  // the shared-memory opt-in is made once per device
@@ -634,29 +757,36 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, kWin>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   const int sms = num_sms_of_current_device();
   if (sms <= 0) return cudaErrorInvalidDevice;
   uint32_t* ws = static_cast<uint32_t*>(a.workspace);
-  attn_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.cu_seqlens, a.num_segments, a.capacity,
-                                                   a.max_seqlen, a.num_heads, ws, a.err);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // short segments: one CTA per SM (one fits per SM by shared memory and TMEM) looping over
-  // items; long segments: one CTA per item.  Never more CTAs than the largest possible number
-  // of items (CTAs past the actual count leave at once).
-  const long long max_items =
-      (static_cast<long long>(a.capacity) / kRowsPerItem + a.num_segments) * a.num_heads;
-  const long long want = a.max_seqlen <= kPersistMaxSeqlen ? sms : max_items;
+  long long max_items, want;
+  if (kWin) {
+    // windows hold at most 256 rows: one CTA per SM looping over (window, head) items
+    max_items = static_cast<long long>(a.wg.nwin[0]) * a.wg.nwin[1] * a.wg.nwin[2] * a.num_heads;
+    want = sms;
+  } else {
+    attn_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.cu_seqlens, a.num_segments, a.capacity,
+                                                     a.max_seqlen, a.num_heads, ws, a.err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // short segments: one CTA per SM (one fits per SM by shared memory and TMEM) looping over
+    // items; long segments: one CTA per item.  Never more CTAs than the largest possible number
+    // of items (CTAs past the actual count leave at once).
+    max_items = (static_cast<long long>(a.capacity) / kRowsPerItem + a.num_segments) * a.num_heads;
+    want = a.max_seqlen <= kPersistMaxSeqlen ? sms : max_items;
+  }
+  if (max_items <= 0) return cudaSuccess;
   const int grid = static_cast<int>(max_items < want ? max_items : want);
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  attn_fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(
+  attn_fwd_kernel<D, kWin><<<grid, kThreads, C::kSmemBytes, stream>>>(
       a.tmap_q, a.tmap_k, a.tmap_v, static_cast<__nv_bfloat16*>(a.o), a.lse, a.cu_seqlens,
-      a.num_segments, a.capacity, a.num_heads, a.scale, scale_log2, ws, a.err);
+      a.num_segments, a.capacity, a.num_heads, a.scale, scale_log2, ws, a.wg, a.err);
   return cudaGetLastError();
 }
 
@@ -668,9 +798,13 @@ size_t attn_workspace_bytes(int num_segments) {
 }
 
 cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t stream) {
+  if (a.window) {
+    if (a.head_dim == 128) return launch<128, true>(a, stream);
+    return launch<64, true>(a, stream);
+  }
   if (a.max_seqlen <= 0 || a.num_segments <= 0) return cudaSuccess;
-  if (a.head_dim == 128) return launch<128>(a, stream);
-  return launch<64>(a, stream);
+  if (a.head_dim == 128) return launch<128, false>(a, stream);
+  return launch<64, false>(a, stream);
 }
 
 }  // namespace h3

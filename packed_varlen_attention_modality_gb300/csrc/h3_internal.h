@@ -48,8 +48,21 @@ cudaError_t launch_window_unpack(const int32_t* perm, int num_tokens, const void
                                  int row_bytes, unsigned int* err, cudaStream_t stream);
 
 // ---- attention ------------------------------------------------------------------------------
+// Window attention straight on the (T, H, W) grid: windows of win[] cut with shift[] (edge
+// windows cropped), frames_per_tile = 128 / (win[1] * win[2]) frames of a window per 128-row tile.
+struct WindowAttnGeom {
+  int L[3];
+  int w[3];
+  int s[3];
+  int nwin[3];
+  int frames_per_tile;
+};
+
 struct AttnArgs {
-  CUtensorMap tmap_q, tmap_k, tmap_v;  // 3-D views {D, H, capacity} of Q, K, V
+  // packed: 3-D views {D, H, capacity} of Q, K, V; window: 5-D views {D, H, W, Hgrid, T}
+  CUtensorMap tmap_q, tmap_k, tmap_v;
+  bool window;
+  WindowAttnGeom wg;
   void* o;
   float* lse;
   const int32_t* cu_seqlens;

@@ -81,6 +81,28 @@ bool make_qkv_map(CUtensorMap* m, const void* base, int rows, int heads, int hea
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 5-D view {D, heads, W, H, T} of a bf16 [T*H*W, heads, D] tensor in row-major token order; box
+// {64, 1, win_w, win_h, frames} (one 128-row tile of a window), 128-byte swizzle.  Coordinates
+// outside the grid (edge windows) read as zero.
+bool make_window_map(CUtensorMap* m, const void* base, const int32_t grid[3], const int32_t win[3],
+                     int frames, int heads, int head_dim) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t row = static_cast<cuuint64_t>(heads) * head_dim * 2;
+  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(grid[2]), static_cast<cuuint64_t>(grid[1]),
+                              static_cast<cuuint64_t>(grid[0])};
+  const cuuint64_t strides[4] = {static_cast<cuuint64_t>(head_dim) * 2, row, row * grid[2],
+                                 row * grid[2] * grid[1]};
+  const cuuint32_t box[5] = {64, 1, static_cast<cuuint32_t>(win[2]), static_cast<cuuint32_t>(win[1]),
+                             static_cast<cuuint32_t>(frames)};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool device_is_sm103() {
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
@@ -291,6 +313,55 @@ h3_status h3_varlen_attn_fwd_noalloc(const void* q, const void* k, const void* v
   a.head_dim = head_dim;
   a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(head_dim));
   a.workspace = scratch;  // the plan kernel rewrites every word the attention kernel reads
+  a.err = device_error_ptr();
+  if (a.err == nullptr) return H3_ERR_CUDA;
+  return from_cuda(h3::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+h3_status h3_window_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const int32_t grid[3], const int32_t win[3], const int32_t shift[3],
+                             int32_t num_heads, int32_t head_dim, float softmax_scale,
+                             h3_stream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || grid == nullptr ||
+      win == nullptr || shift == nullptr)
+    return H3_ERR_NULL;
+  const int32_t nwin = h3_window_count(grid, win, shift);
+  if (nwin < 0 || num_heads <= 0) return H3_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return H3_ERR_UNSUPPORTED;
+  // a 128-row tile is whole frames of a window, and a window is at most two tiles
+  const int per_frame = win[1] * win[2];
+  if (per_frame > 128 || 128 % per_frame != 0 || win[0] * per_frame > 256 || win[1] > 256 ||
+      win[2] > 256)
+    return H3_ERR_UNSUPPORTED;
+  if (!(softmax_scale <= 0.f || std::isfinite(softmax_scale))) return H3_ERR_INVALID_ARG;
+  const int64_t n = static_cast<int64_t>(grid[0]) * grid[1] * grid[2];
+  if (n > INT32_MAX / 2 || static_cast<int64_t>(nwin) * num_heads > INT32_MAX)
+    return H3_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return H3_ERR_MISALIGNED;
+  if (!device_is_sm103()) return H3_ERR_UNSUPPORTED;
+
+  h3::AttnArgs a{};
+  a.window = true;
+  const int frames = 128 / per_frame;
+  for (int ax = 0; ax < 3; ++ax) {
+    a.wg.L[ax] = grid[ax];
+    a.wg.w[ax] = win[ax];
+    a.wg.s[ax] = shift[ax];
+    a.wg.nwin[ax] = (grid[ax] + shift[ax] + win[ax] - 1) / win[ax];
+  }
+  a.wg.frames_per_tile = frames;
+  if (!make_window_map(&a.tmap_q, q, grid, win, frames, num_heads, head_dim) ||
+      !make_window_map(&a.tmap_k, k, grid, win, frames, num_heads, head_dim) ||
+      !make_window_map(&a.tmap_v, v, grid, win, frames, num_heads, head_dim))
+    return H3_ERR_CUDA;
+  a.o = o;
+  a.lse = lse;
+  a.capacity = static_cast<int>(n);  // LSE row stride: [heads, T*H*W]
+  a.num_heads = num_heads;
+  a.head_dim = head_dim;
+  a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(head_dim));
   a.err = device_error_ptr();
   if (a.err == nullptr) return H3_ERR_CUDA;
   return from_cuda(h3::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));

@@ -100,6 +100,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,
+                                            int32_t c2, int32_t c3, int32_t c4, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "r"(bar)
+      : "memory");
+}
+
 // ---------------------------------------------------------------------------------------------
 // tcgen05: tensor memory allocation, MMA, commit, TMEM <-> register moves.
 // ---------------------------------------------------------------------------------------------

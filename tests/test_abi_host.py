@@ -139,3 +139,19 @@ def test_window_calls_reject_bad_arguments_on_the_host(lib):
     assert lib.h3_window_unpack(P(FAKE), 16, P(FAKE + 8), P(FAKE), 256, None) == 8
     assert lib.h3_window_unpack(None, 16, P(FAKE), P(FAKE), 256, None) == 1
     assert lib.h3_window_unpack(P(FAKE), -2, P(FAKE), P(FAKE), 256, None) == 2
+
+
+def test_window_attention_rejects_bad_arguments_on_the_host(lib):
+    P = ctypes.c_void_p
+    f = lib.h3_window_attn_fwd
+    g, w, sh = _i3((4, 8, 8)), _i3((4, 8, 8)), _i3((2, 4, 4))
+
+    def call(q=FAKE, win=w, H=2, D=128, grid=g, shift=sh):
+        return f(P(q) if q else None, P(FAKE), P(FAKE), P(FAKE), None, grid, win, shift, H, D, 0.0, None)
+
+    assert call(q=0) == 1
+    assert call(H=0) == 2 and call(shift=_i3((4, 0, 0))) == 2
+    assert call(D=96) == 4
+    assert call(win=_i3((4, 8, 12))) == 4   # 8*12 does not divide 128
+    assert call(win=_i3((8, 8, 8))) == 4    # 512 rows: more than two 128-row tiles
+    assert call(q=FAKE + 8) == 8

@@ -324,3 +324,60 @@ def test_unpack_reports_bad_perm(h3, dev):
     ok = torch.ones(n, dtype=torch.bool)
     ok[5] = False
     assert torch.equal(dst[ok.to(dev)], src[ok.to(dev)])
+
+
+# ---------------------------------------------------------------------------------------------
+# window attention in place on the grid (no packed copies)
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("layer", [0, 1])
+def test_window_attention_in_place_matches_oracle_and_packed_path(h3, dev, window_case, layer):
+    wl = window_case
+    shift = wl.shift if wl.layer_shifted[layer] else (0, 0, 0)
+    q, k, v = (t.to(dev) for t in wl.layers[layer])
+    o, lse = h3.window_attn_fwd(q, k, v, wl.grid, wl.window, shift, return_lse=True)
+    perm, cu, (qp, kp, vp) = h3.window_pack(wl.grid, wl.window, shift, [q, k, v])
+    op, lsep = h3.varlen_attn_fwd(qp, kp, vp, cu, 256, return_lse=True)
+    o_packed = h3.window_unpack(perm, op)
+    torch.cuda.synchronize()
+    assert h3.get_device_error(dev) == 0
+    # every row against the packed GPU path (different key order inside the tiles)
+    _close(o.float().cpu().numpy(), o_packed.float().cpu().numpy(), f"in place vs packed, layer {layer}")
+    lse_packed = torch.empty_like(lse)
+    lse_packed[:, perm.long()] = lsep
+    _lse_close(lse.cpu().numpy(), lse_packed.cpu().numpy(), f"in place vs packed, layer {layer}")
+    # sampled windows against the oracle, in original order
+    p_ref, cu_ref = oracle.window_partition(wl.grid, wl.window, shift)
+    nwin = len(cu_ref) - 1
+    rng = np.random.default_rng(70 + layer)
+    wins = np.unique(np.concatenate([[0, 1, nwin - 1, nwin // 2], rng.choice(nwin, 40, replace=False)]))
+    o_cpu, lse_cpu = o.cpu(), lse.cpu()
+    qc, kc, vc = wl.layers[layer]
+    for wdx in wins:
+        a, b = int(cu_ref[wdx]), int(cu_ref[wdx + 1])
+        members = p_ref[a:b].astype(np.int64)
+        ref_o, ref_lse = oracle.varlen_attention(qc[members], kc[members], vc[members], [0, b - a])
+        _close(o_cpu[members].float().numpy(), ref_o, f"in place window {wdx} layer {layer}")
+        _lse_close(lse_cpu[:, members].numpy(), ref_lse, f"in place window {wdx} layer {layer}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("grid,win,shift", [((5, 9, 11), (4, 8, 8), (2, 4, 4)),
+                                            ((3, 16, 8), (2, 8, 8), (1, 4, 0)),
+                                            ((6, 7, 5), (4, 4, 8), (0, 2, 3))])
+def test_window_attention_in_place_small_grids_full_oracle(h3, dev, D, grid, win, shift):
+    n = grid[0] * grid[1] * grid[2]
+    rng = np.random.default_rng(n + D)
+    q, k, v = (torch.from_numpy(rng.standard_normal((n, 3, D)).astype(np.float32)).to(torch.bfloat16)
+               for _ in range(3))
+    o, lse = h3.window_attn_fwd(q.to(dev), k.to(dev), v.to(dev), grid, win, shift, return_lse=True)
+    torch.cuda.synchronize()
+    assert h3.get_device_error(dev) == 0
+    perm, cu = oracle.window_partition(grid, win, shift)
+    ref_o, ref_lse = oracle.varlen_attention(oracle.window_pack(q, perm), oracle.window_pack(k, perm),
+                                             oracle.window_pack(v, perm), cu)
+    ref_o = oracle.window_unpack(ref_o, perm)
+    ref_lse_orig = np.empty_like(ref_lse)
+    ref_lse_orig[:, perm] = ref_lse
+    _close(o.float().cpu().numpy(), ref_o, f"in place {grid} {win} {shift} D {D}")
+    _lse_close(lse.cpu().numpy(), ref_lse_orig, f"in place {grid} {win} {shift} D {D}")
