@@ -15,7 +15,9 @@ Sources (page title + section):
              "Crossing the time boundary", step 3 "RoPE global time alignment"
              (t_global = t_local + s*40/24, time axis only, decimals kept);
              "Breaking the memory wall: window attention across GPUs" (regular and half-shifted
-             3D windows, edge windows cropped, token order restored afterwards).
+             3D windows, edge windows cropped, token order restored afterwards);
+             "VSA: block-sparse attention" (64-token 4x4x4 blocks, block-level gated scoring,
+             top-k block selection, token-level attention between the selected blocks).
 
 Every function here is pinned by tests/test_oracle_pins.py against closed forms, textbook
 routines, brute force and the pages' printed examples.  Readings where the pages are silent
@@ -26,10 +28,13 @@ from .rope import (continuation_time_shift, rope_inv_freq, rope_angles, rope_app
                    video_axis_split)
 from .window import (axis_window_count, window_count, window_ids, window_partition,
                      window_pack, window_unpack)
+from .vsa import (vsa_block_counts, vsa_block_count, vsa_block_ids, vsa_block_means,
+                  vsa_block_scores, vsa_select, vsa_attention)
 
 __all__ = [
     "varlen_attention", "attention_weights", "dense_masked_attention_bruteforce",
     "continuation_time_shift", "rope_inv_freq", "rope_angles", "rope_apply", "video_axis_split",
     "axis_window_count", "window_count", "window_ids", "window_partition", "window_pack",
-    "window_unpack",
+    "window_unpack", "vsa_block_counts", "vsa_block_count", "vsa_block_ids", "vsa_block_means",
+    "vsa_block_scores", "vsa_select", "vsa_attention",
 ]
