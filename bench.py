@@ -43,7 +43,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--workload", default="h3_full_request",
                    choices=["h3_full_request", "single_request_4k", "continuation_batch",
-                            "video_segment_16k", "window_grid", "window_grid_16x24x84"],
+                            "video_segment_16k", "window_grid", "window_grid_16x24x84",
+                            "vsa_video", "vsa_video_16x24x84"],
                    help="h3_full_request is the metric's workload; the others are side measurements")
     return p.parse_args()
 
@@ -226,6 +227,8 @@ def run_ours(args, rank, world, local_rank):
     peaks = load_peaks()
     if args.workload.startswith("window_grid"):
         return run_window(args, rank, world, dev, h3, peaks)
+    if args.workload.startswith("vsa_video"):
+        return run_vsa(args, rank, world, dev, h3, peaks)
     headline = args.workload == "h3_full_request"
     wl = workloads.WORKLOADS[args.workload]()
     H, D, C, N = wl.num_heads, wl.head_dim, wl.capacity, wl.num_tokens
@@ -357,7 +360,7 @@ def run_ours(args, rank, world, local_rank):
                                  "frac_hbm": rope_gbs / peaks["hbm_gbs"]},
                         "attn_fwd": {"ms": attn_ms, "tflops": attn_tflops}},
             "clocks": clocks,
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": 3 * args.steps,   # RoPE, attention plan, attention per step
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
@@ -497,6 +500,89 @@ def run_window(args, rank, world, dev, h3, peaks):
                        "l2": "inputs larger than L2 (%d MB per tensor)" % round(n * row / 1e6)},
             "layers": per, "roofline": roofline, "clocks": clocks,
             "gpu_launches": 2 * args.steps}), flush=True)
+
+
+def run_vsa(args, rank, world, dev, h3, peaks):
+    """Block-sparse video attention on the 1344x768 latent (32x48x84 grid, 4x4x4 blocks = 2016,
+    top 252 = 1/8; 24 heads x 128): per step the block gate + top-k selection, then the attention
+    of every query block over its selected blocks.  vsa_video_16x24x84 is a quarter of the grid
+    for full ncu captures."""
+    from workloads import vsa_video
+
+    wl = vsa_video(grid=(16, 24, 84), topk=126) if args.workload == "vsa_video_16x24x84" else vsa_video()
+    n, H, D = wl.num_tokens, wl.num_heads, wl.head_dim
+    q, k, v = wl.q.to(dev), wl.k.to(dev), wl.v.to(dev)
+    del wl.q, wl.k, wl.v
+    nblk = h3.vsa_block_count(wl.grid, wl.block)
+    scores = torch.empty((H, nblk, nblk), dtype=torch.float32, device=dev)
+    sel = torch.empty((H, nblk, wl.topk), dtype=torch.int32, device=dev)
+    ws = torch.empty(h3.vsa_select_workspace_size(wl.grid, wl.block, H, D), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        h3.vsa_select(q, k, wl.grid, wl.topk, block=wl.block, scores=scores, out=sel, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+        h3.vsa_attn_fwd(q, k, v, wl.grid, sel, block=wl.block, out=o)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if h3.get_device_error(dev) != 0:
+        raise RuntimeError("device error during warm-up")
+    # useful attention FLOPs from the selection: 4 H D sum_a n_a sum_{b in sel(a)} n_b
+    sizes = torch.tensor(_block_sizes(wl.grid, wl.block), dtype=torch.float64, device=dev)
+    flops = float(4.0 * D * (sizes[None, :, None] * sizes[sel.long()]).sum().item())
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if h3.get_device_error(dev) != 0:
+        raise RuntimeError("device error during the timed steps")
+    ms_per_step = max_over_ranks(t0.elapsed_time(t1) / args.steps, world, dev)
+    sel_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    attn_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    attn_tflops = flops / attn_ms / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "block-sparse video attention TFLOP/s (gate + top-k + attention over selected blocks)",
+            "value": job_throughput(flops, world, ms_per_step), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "tokens": n, "heads": H, "head_dim": D, "blocks": nblk,
+                       "topk": wl.topk, "attention_flop_useful": flops,
+                       "l2": "inputs larger than L2 (%d MB per tensor)" % round(n * H * D * 2 / 1e6)},
+            "kernels": {"select": {"ms": sel_ms, "note": "block means + fp32 score GEMM + radix top-k"},
+                        "attn": {"ms": attn_ms, "tflops_useful": attn_tflops,
+                                 "tflops_executed": 2 * attn_tflops,
+                                 "note": "each 128-row tile holds two query blocks with their own key "
+                                         "blocks: half of every MMA is masked work"}},
+            "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": attn_tflops / peaks["bf16_tflops"], "traffic": None,
+                         "kernel": "attn_fwd_kernel<%d, vsa>" % D,
+                         "peak_source": peaks["source"] + " bf16_tflops (burst)",
+                         "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"]},
+            "clocks": clocks, "gpu_launches": 4 * args.steps}), flush=True)
+
+
+def _block_sizes(grid, block):
+    """Tokens per block (edge blocks cropped), in block-id order -- host bookkeeping for FLOPs."""
+    axes = [np.array([min(b, L - b * i) for i in range((L + b - 1) // b)]) for L, b in zip(grid, block)]
+    return np.einsum("i,j,k->ijk", *axes).reshape(-1)
 
 
 def _kernel_sha():

@@ -62,7 +62,8 @@ typedef enum {
   H3_ERR_CUDA = 6,            /* a CUDA runtime / driver call failed */
   H3_ERR_TIMEOUT = 7,         /* (device) a bounded wait inside a kernel ran out */
   H3_ERR_MISALIGNED = 8,      /* a device pointer or row size is not 16-byte aligned */
-  H3_ERR_BAD_PERM = 9         /* (device) a permutation entry is out of range */
+  H3_ERR_BAD_PERM = 9,        /* (device) a permutation entry is out of range */
+  H3_ERR_BAD_BLOCK_INDEX = 10 /* (device) a selected VSA block index is out of range */
 } h3_status;
 
 enum { H3_TAG_TEXT = 0, H3_TAG_VIDEO = 1, H3_TAG_AUDIO = 2 };
@@ -227,6 +228,63 @@ H3_API h3_status h3_window_attn_fwd(const void* q, const void* k, const void* v,
  * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG, H3_ERR_MISALIGNED, H3_ERR_CUDA. */
 H3_API h3_status h3_window_unpack(const int32_t* perm, int32_t num_tokens, const void* src, void* dst,
                            int32_t row_bytes, h3_stream_t stream);
+
+/* ---- Block-sparse video attention (VSA) ----------------------------------------------------
+ * [H3-fast] "Breaking the engineering bottlenecks of video-generation models", section "VSA:
+ * block-sparse attention": the video latent is cut into 4x4x4 = 64-token blocks along time,
+ * height and width; a block-level gate scores each key block against the query block and only
+ * the top-k blocks enter a token-level attention between the selected blocks.  The pages leave
+ * the gate and k open: here the gate score of key block b for query block a (per head) is
+ * scale * <mean of a's query rows, mean of b's key rows>, means over the block's tokens inside the
+ * grid; k is the caller's.
+ *
+ * Layout shared by the VSA calls: q, k, v, o are device bf16 [T*H*W, num_heads, head_dim] in
+ * row-major (t, h, w) token order (the layout of h3_window_attn_fwd).  Blocks are cut at
+ * multiples of block[] from the origin (no shift), edge blocks cropped by the grid; block id
+ * = (i_t * nb_h + i_h) * nb_w + i_w with nb_a = ceil(grid[a] / block[a]).
+ * Supported: block[0] * block[1] * block[2] == 64 (e.g. 4x4x4), head_dim 64 or 128; else
+ * H3_ERR_UNSUPPORTED. */
+
+/* Number of blocks: prod ceil(grid[a] / block[a]); -1 for a non-positive size or overflow. */
+H3_API int32_t h3_vsa_block_count(const int32_t grid[3], const int32_t block[3]);
+
+/* Workspace bytes of h3_vsa_select (the block means of Q and K, fp32); 0 for invalid sizes. */
+H3_API size_t h3_vsa_select_workspace_size(const int32_t grid[3], const int32_t block[3],
+                                           int32_t num_heads, int32_t head_dim);
+
+/* Block gate scores and top-k block selection.
+ * q, k       : device bf16 [T*H*W, num_heads, head_dim] (layout above); 16-byte aligned.
+ * topk       : selected key blocks per query block, 1 <= topk <= nblk.
+ * softmax_scale: scale of the gate scores; <= 0 selects 1/sqrt(head_dim).
+ * scores     : device fp32 [num_heads, nblk, nblk] out, caller-owned: the gate scores.
+ * block_idx  : device int32 [num_heads, nblk, topk] out: for each head and query block, the
+ *              topk key blocks with the highest scores (equal scores: lower block id first),
+ *              listed in ascending block id.
+ * workspace  : device, >= h3_vsa_select_workspace_size() bytes, 16-byte aligned.
+ * Scores are accumulated in fp32 (block means in token order, dot products in dimension order),
+ * so blocks whose scores differ by fp32 rounding may be taken in either order.  Inputs must be
+ * finite.
+ * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG, H3_ERR_UNSUPPORTED, H3_ERR_WORKSPACE,
+ *         H3_ERR_MISALIGNED, H3_ERR_CUDA. */
+H3_API h3_status h3_vsa_select(const void* q, const void* k, const int32_t grid[3],
+                               const int32_t block[3], int32_t num_heads, int32_t head_dim,
+                               int32_t topk, float softmax_scale, float* scores, int32_t* block_idx,
+                               void* workspace, size_t workspace_bytes, h3_stream_t stream);
+
+/* Token-level attention over the selected blocks: query i of block a attends, with one softmax,
+ * to every key row of the blocks block_idx[h][a][0..topk) (rows inside the grid only).
+ * q, k, v, o : device bf16 [T*H*W, num_heads, head_dim] (layout above); o gets every row.
+ * lse        : device fp32 [num_heads, T*H*W] (natural log) or NULL.
+ * block_idx  : device int32 [num_heads, nblk, topk], e.g. from h3_vsa_select; any order, ids
+ *              distinct per list (a repeated id counts its keys twice).  An id outside [0, nblk)
+ *              is replaced by block 0 and recorded as H3_ERR_BAD_BLOCK_INDEX.
+ * softmax_scale: <= 0 selects 1/sqrt(head_dim).  No workspace.
+ * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG, H3_ERR_UNSUPPORTED, H3_ERR_MISALIGNED, H3_ERR_CUDA;
+ *         device-side H3_ERR_BAD_BLOCK_INDEX / H3_ERR_TIMEOUT. */
+H3_API h3_status h3_vsa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 const int32_t grid[3], const int32_t block[3], int32_t num_heads,
+                                 int32_t head_dim, const int32_t* block_idx, int32_t topk,
+                                 float softmax_scale, h3_stream_t stream);
 
 /* Synchronises `stream`, returns the first device-side error recorded on the current device
  * since the last call (H3_OK if none) and clears it. */

@@ -60,10 +60,11 @@ def vsa_block_means(x, grid: Sequence[int], block: Sequence[int]) -> np.ndarray:
     N, H, D = xa.shape
     ids = vsa_block_ids(grid, block)
     nblk = vsa_block_count(grid, block)
-    sums = np.zeros((nblk, H, D), dtype=np.float64)
-    np.add.at(sums, ids, xa)
-    counts = np.bincount(ids, minlength=nblk).astype(np.float64)
-    return np.transpose(sums / counts[:, None, None], (1, 0, 2))
+    order = np.argsort(ids, kind="stable")                 # rows grouped by block
+    counts = np.bincount(ids, minlength=nblk)              # every block holds >= 1 row
+    starts = np.concatenate([[0], np.cumsum(counts)[:-1]])
+    sums = np.add.reduceat(xa[order], starts, axis=0)      # [nblk, H, D]
+    return np.transpose(sums / counts[:, None, None].astype(np.float64), (1, 0, 2))
 
 
 def vsa_block_scores(q, k, grid: Sequence[int], block: Sequence[int],
@@ -74,7 +75,7 @@ def vsa_block_scores(q, k, grid: Sequence[int], block: Sequence[int],
     D = qm.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    return scale * np.einsum("had,hbd->hab", qm, km)
+    return scale * np.matmul(qm, np.transpose(km, (0, 2, 1)))
 
 
 def vsa_select(scores: np.ndarray, topk: int) -> np.ndarray:

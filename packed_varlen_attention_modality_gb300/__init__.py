@@ -10,6 +10,8 @@ Calls:
   varlen_attn_fwd   block-diagonal softmax attention over cu_seqlens segments
   window_count / window_pack / window_unpack   shifted 3D window partition and row gather/scatter
   window_attn_fwd   shifted 3D window attention read and written in place on the grid
+  vsa_select / vsa_attn_fwd   block-sparse video attention: block gate scores + top-k
+                    selection, then attention over the selected 64-token blocks
   get_device_error  read (and clear) the device-side error word
 """
 from __future__ import annotations
@@ -21,7 +23,8 @@ from typing import Optional, Sequence, Tuple
 import torch
 
 __all__ = ["H3Error", "RopeConfig", "lib_path", "load_library", "rope_apply", "varlen_attn_fwd",
-           "varlen_attn_fwd_noalloc", "window_attn_fwd",
+           "varlen_attn_fwd_noalloc", "window_attn_fwd", "vsa_block_count",
+           "vsa_select_workspace_size", "vsa_select", "vsa_attn_fwd",
            "varlen_attn_workspace_size", "window_count", "window_pack", "window_unpack",
            "get_device_error", "TAG_TEXT", "TAG_VIDEO", "TAG_AUDIO"]
 
@@ -33,7 +36,7 @@ _lib = None
 
 _STATUS = {0: "H3_OK", 1: "H3_ERR_NULL", 2: "H3_ERR_INVALID_ARG", 3: "H3_ERR_BAD_CU_SEQLENS",
            4: "H3_ERR_UNSUPPORTED", 5: "H3_ERR_WORKSPACE", 6: "H3_ERR_CUDA", 7: "H3_ERR_TIMEOUT",
-           8: "H3_ERR_MISALIGNED", 9: "H3_ERR_BAD_PERM"}
+           8: "H3_ERR_MISALIGNED", 9: "H3_ERR_BAD_PERM", 10: "H3_ERR_BAD_BLOCK_INDEX"}
 
 
 class H3Error(RuntimeError):
@@ -79,6 +82,10 @@ def load_library():
         "h3_window_pack": (I32, [I32P, I32P, I32P, P, P, ctypes.POINTER(P), ctypes.POINTER(P),
                                  I32, I32, P]),
         "h3_window_unpack": (I32, [P, I32, P, P, I32, P]),
+        "h3_vsa_block_count": (I32, [I32P, I32P]),
+        "h3_vsa_select_workspace_size": (U64, [I32P, I32P, I32, I32]),
+        "h3_vsa_select": (I32, [P, P, I32P, I32P, I32, I32, I32, F32, P, P, P, U64, P]),
+        "h3_vsa_attn_fwd": (I32, [P, P, P, P, P, I32P, I32P, I32, I32, P, I32, F32, P]),
         "h3_get_device_error": (I32, [P]),
         "h3_status_string": (ctypes.c_char_p, [I32]),
         "h3_version": (I32, []),
@@ -348,6 +355,97 @@ def window_unpack(perm: torch.Tensor, src: torch.Tensor, out: Optional[torch.Ten
         st = lib.h3_window_unpack(_ptr(perm), n, _ptr(src), _ptr(out), row_bytes, _stream(dev))
     _check(st, "h3_window_unpack")
     return out
+
+
+def vsa_block_count(grid: Sequence[int], block: Sequence[int] = (4, 4, 4)) -> int:
+    n = load_library().h3_vsa_block_count(_i3(grid), _i3(block))
+    if n < 0:
+        raise ValueError("invalid VSA block geometry")
+    return int(n)
+
+
+def vsa_select_workspace_size(grid: Sequence[int], block: Sequence[int], num_heads: int,
+                              head_dim: int) -> int:
+    return int(load_library().h3_vsa_select_workspace_size(_i3(grid), _i3(block), num_heads, head_dim))
+
+
+def vsa_select(q: torch.Tensor, k: torch.Tensor, grid: Sequence[int], topk: int,
+               block: Sequence[int] = (4, 4, 4), scores: Optional[torch.Tensor] = None,
+               out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+               softmax_scale: Optional[float] = None):
+    """Block gate scores and top-k key blocks per query block (VSA).
+
+    q, k: bf16 [T*H*W, heads, D] in row-major (t, h, w) order.  Returns (block_idx int32
+    [heads, nblk, topk] in ascending block id, scores fp32 [heads, nblk, nblk]).
+    """
+    dev = q.device
+    _require(q, "q", torch.bfloat16, dev)
+    _require(k, "k", torch.bfloat16, dev)
+    n = int(grid[0]) * int(grid[1]) * int(grid[2])
+    if q.dim() != 3 or q.shape[0] != n or k.shape != q.shape:
+        raise ValueError("q, k must be [T*H*W, heads, D]")
+    _, H, D = q.shape
+    nblk = vsa_block_count(grid, block)
+    if scores is None:
+        scores = torch.empty((H, nblk, nblk), dtype=torch.float32, device=dev)
+    if out is None:
+        out = torch.empty((H, nblk, int(topk)), dtype=torch.int32, device=dev)
+    _require(scores, "scores", torch.float32, dev)
+    _require(out, "out", torch.int32, dev)
+    if tuple(scores.shape) != (H, nblk, nblk) or tuple(out.shape) != (H, nblk, int(topk)):
+        raise ValueError("scores must be [heads, nblk, nblk] and out [heads, nblk, topk]")
+    need = vsa_select_workspace_size(grid, block, H, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _require(workspace, "workspace", torch.uint8, dev)
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        st = lib.h3_vsa_select(_ptr(q), _ptr(k), _i3(grid), _i3(block), H, D, int(topk), scale,
+                               _ptr(scores), _ptr(out), _ptr(workspace), workspace.numel(),
+                               _stream(dev))
+    _check(st, "h3_vsa_select")
+    return out, scores
+
+
+def vsa_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grid: Sequence[int],
+                 block_idx: torch.Tensor, block: Sequence[int] = (4, 4, 4),
+                 out: Optional[torch.Tensor] = None, return_lse: bool = False,
+                 lse: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None):
+    """Token-level attention of every query block over its selected key blocks (VSA).
+
+    q, k, v: bf16 [T*H*W, heads, D] in row-major (t, h, w) order; block_idx int32
+    [heads, nblk, topk].  Returns out (and lse fp32 [heads, T*H*W] when requested).
+    """
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name, torch.bfloat16, dev)
+    n = int(grid[0]) * int(grid[1]) * int(grid[2])
+    if q.dim() != 3 or q.shape[0] != n or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must be [T*H*W, heads, D]")
+    _, H, D = q.shape
+    nblk = vsa_block_count(grid, block)
+    _require(block_idx, "block_idx", torch.int32, dev)
+    if block_idx.dim() != 3 or tuple(block_idx.shape[:2]) != (H, nblk):
+        raise ValueError("block_idx must be [heads, nblk, topk]")
+    topk = int(block_idx.shape[2])
+    out = torch.empty_like(q) if out is None else out
+    _require(out, "out", torch.bfloat16, dev)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if return_lse and lse is None:
+        lse = torch.empty((H, n), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _require(lse, "lse", torch.float32, dev)
+        if tuple(lse.shape) != (H, n):
+            raise ValueError("lse must be [heads, T*H*W]")
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        st = lib.h3_vsa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _i3(grid),
+                                 _i3(block), H, D, _ptr(block_idx), topk, scale, _stream(dev))
+    _check(st, "h3_vsa_attn_fwd")
+    return (out, lse) if (return_lse or lse is not None) else out
 
 
 def get_device_error(device: Optional[torch.device] = None) -> int:

@@ -68,6 +68,11 @@ constexpr int kSortMax = 256;         // segments ordered longest-first up to th
 constexpr int kWsHeader = 4;          // workspace words: (spare), total items, 2 spare
 constexpr int kPersistMaxSeqlen = 2048;  // loop over items per CTA up to this segment length
 
+constexpr int kModePacked = kAttnModePacked;  // kernel variants (see h3_internal.h)
+constexpr int kModeWindow = kAttnModeWindow;
+constexpr int kModeVsa = kAttnModeVsa;
+constexpr int kVsaBlockRows = 64;  // rows of one VSA block = half a 128-row tile
+
 // Workspace (uint32 words): [1] total items, [kWsHeader, +S) segment order,
 // [kWsHeader + S, +S+1) exclusive prefix of items in that order.
 __host__ __device__ constexpr size_t workspace_words(int num_segments) {
@@ -80,7 +85,8 @@ struct WorkDesc {
   int head;
   int q0;         // packed: first query row of the item
   int box[3];     // window: grid (t, h, w) of the first valid tile's box origin (may be < 0)
-  int ntiles;     // window: valid 128-row tiles of the window (1 or 2)
+  int ntiles;     // window / VSA: query tiles of the item (1 or 2)
+  int nkv;        // window / VSA: key/value steps of the item
   uint32_t mask[2][4];  // window: rows of each tile that lie inside the grid (= inside the window)
 };
 
@@ -90,9 +96,9 @@ struct ItemShape {
   int kv_last_valid;  // keys in the last key tile (packed; 128 for windows, which use masks)
 };
 
-template <bool kWin>
+template <int kMode>
 __device__ __forceinline__ ItemShape shape_of(const WorkDesc& d) {
-  if (kWin) return ItemShape{d.ntiles == 2, d.ntiles, kBlockN};
+  if (kMode != kModePacked) return ItemShape{d.ntiles == 2, d.nkv, kBlockN};
   const int nkv = (d.seg_len + kBlockN - 1) / kBlockN;
   return ItemShape{d.q0 + kBlockM < d.seg_start + d.seg_len, nkv, d.seg_len - (nkv - 1) * kBlockN};
 }
@@ -134,6 +140,7 @@ __device__ __forceinline__ WorkDesc decode_window(uint32_t item, const WindowAtt
   const int bt = g.frames_per_tile;
   const int tile_lo = vl_t / bt, tile_hi = (vh_t + bt - 1) / bt;
   d.ntiles = tile_hi - tile_lo;
+  d.nkv = d.ntiles;
   d.box[0] = lo_t + tile_lo * bt;
   d.box[1] = lo_h;
   d.box[2] = lo_w;
@@ -157,6 +164,54 @@ __device__ __forceinline__ WorkDesc decode_window(uint32_t item, const WindowAtt
     d.mask[k][3] = static_cast<uint32_t>(thi >> 32);
   }
   return d;
+}
+
+// ---- VSA: blocks of 64 tokens (bt x bh x bw) cut from the grid at multiples of the block size.
+// wg.w[] holds the block size, wg.nwin[] the blocks per axis, wg.topk the selected key blocks per
+// query block; block b = (i_t, i_h, i_w) lexicographic.
+__device__ __forceinline__ int vsa_num_blocks(const WindowAttnGeom& g) {
+  return g.nwin[0] * g.nwin[1] * g.nwin[2];
+}
+// Grid origin (t, h, w) of block b.
+__device__ __forceinline__ void vsa_block_origin(int b, const WindowAttnGeom& g, int& t0, int& h0,
+                                                 int& w0) {
+  w0 = (b % g.nwin[2]) * g.w[2];
+  h0 = ((b / g.nwin[2]) % g.nwin[1]) * g.w[1];
+  t0 = (b / (g.nwin[2] * g.nwin[1])) * g.w[0];
+}
+// Rows of block b inside the grid: bit (ft * bh + fh) * bw + fw of a 64-bit mask.
+__device__ __forceinline__ uint64_t vsa_block_mask(int b, const WindowAttnGeom& g) {
+  int t0, h0, w0;
+  vsa_block_origin(b, g, t0, h0, w0);
+  const int nt = min(g.w[0], g.L[0] - t0), nh = min(g.w[1], g.L[1] - h0);
+  const uint64_t run = low_bits(min(g.w[2], g.L[2] - w0));
+  uint64_t frame = 0, m = 0;
+  for (int fh = 0; fh < nh; ++fh) frame |= run << (fh * g.w[2]);
+  for (int ft = 0; ft < nt; ++ft) m |= frame << (ft * g.w[1] * g.w[2]);
+  return m;
+}
+// Item -> descriptor: query blocks q0 .. q0 + 3 of one head (tile t holds blocks q0 + 2t and
+// q0 + 2t + 1 in its two 64-row halves), head fastest.
+__device__ __forceinline__ WorkDesc decode_vsa(uint32_t item, const WindowAttnGeom& g,
+                                               int num_heads) {
+  WorkDesc d{};
+  d.seg_len = 1;
+  d.head = static_cast<int>(item % static_cast<uint32_t>(num_heads));
+  d.q0 = 4 * static_cast<int>(item / static_cast<uint32_t>(num_heads));
+  d.ntiles = d.q0 + 2 < vsa_num_blocks(g) ? 2 : 1;
+  d.nkv = g.topk;
+  return d;
+}
+// Selected key block j of query block qb (head h), checked against the block count.
+__device__ __forceinline__ int vsa_selected(const int32_t* __restrict__ sel, int h, int qb, int j,
+                                            const WindowAttnGeom& g, unsigned int* err) {
+  const int nblk = vsa_num_blocks(g);
+  const int b = __ldg(sel + (static_cast<size_t>(h) * nblk + qb) * g.topk + j);
+  if (b < 0 || b >= nblk) {
+    record_error(err, kErrBadBlockIndex);
+    return 0;
+  }
+  return b;
 }
 
 __device__ __forceinline__ int checked_len(const int32_t* __restrict__ cu, int g, int capacity,
@@ -268,10 +323,13 @@ struct Cfg {
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, true);
 };
 
-// kWin = false: packed varlen segments (cu_seqlens, 3-D tensor maps, rows of [capacity, H, D]).
-// kWin = true: windows of a (T, H, W) grid read in place (5-D tensor maps over [T, H, W, heads, D]
+// kModePacked: packed varlen segments (cu_seqlens, 3-D tensor maps, rows of [capacity, H, D]).
+// kModeWindow: windows of a (T, H, W) grid read in place (5-D tensor maps over [T, H, W, heads, D]
 // in row-major token order); the output goes back to the same positions.
-template <int D, bool kWin>
+// kModeVsa: 64-token blocks of the grid read in place; each 64-row half of a query tile is one
+// query block and attends to its own selected key blocks (vsa_sel), which fill the same half of
+// every key/value tile.  The two query tiles of an item have separate key/value streams.
+template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 const __grid_constant__ CUtensorMap tmap_k,
@@ -279,7 +337,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 float* __restrict__ lse, const int32_t* __restrict__ cu_seqlens, int num_segments,
                 int capacity, int num_heads, float scale, float scale_log2,
                 uint32_t* __restrict__ ws, const __grid_constant__ WindowAttnGeom wg,
-                unsigned int* err) {
+                const int32_t* __restrict__ vsa_sel, unsigned int* err) {
+  constexpr bool kWin = kMode == kModeWindow;
+  constexpr bool kVsa = kMode == kModeVsa;
   using C = Cfg<D>;
   constexpr int SK = C::kStagesK;
   constexpr int SV = C::kStagesV;
@@ -355,8 +415,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     if (warp == 8) {
       // ================= scheduler + TMA producer =================
       if (lane == 0) {
-        const uint32_t total =
-            kWin ? static_cast<uint32_t>(wg.nwin[0] * wg.nwin[1] * wg.nwin[2] * num_heads) : ws[1];
+        uint32_t total;
+        if constexpr (kWin)
+          total = static_cast<uint32_t>(wg.nwin[0] * wg.nwin[1] * wg.nwin[2] * num_heads);
+        else if constexpr (kVsa)
+          total = static_cast<uint32_t>((vsa_num_blocks(wg) + 3) / 4 * num_heads);
+        else
+          total = ws[1];
         uint32_t kt = 0, vt = 0;  // K / V tiles loaded so far (positions in the rings)
         uint32_t qn[2] = {0u, 0u};  // Q tiles loaded so far, per tile slot
         bool ok = true;
@@ -364,8 +429,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           const uint32_t item = blockIdx.x + static_cast<uint32_t>(k) * gridDim.x;
           WorkDesc d;
           if (item < total) {
-            d = kWin ? decode_window(item, wg, num_heads)
-                     : decode_item(item, ws, cu_seqlens, num_segments, num_heads);
+            if constexpr (kWin)
+              d = decode_window(item, wg, num_heads);
+            else if constexpr (kVsa)
+              d = decode_vsa(item, wg, num_heads);
+            else
+              d = decode_item(item, ws, cu_seqlens, num_segments, num_heads);
           } else {
             d.seg_start = 0;
             d.seg_len = -1;
@@ -377,7 +446,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           work[k & 1] = d;
           mbar_arrive(bar_wfull(k & 1));
           if (d.seg_len < 0) break;
-          const ItemShape sh = shape_of<kWin>(d);
+          const ItemShape sh = shape_of<kMode>(d);
           const bool has1 = sh.has1;
           const int nkv = sh.nkv;
           // tile loads: packed rows [row, row + 128) of one head; window box (w, h, t) of frames
@@ -391,28 +460,99 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 tma_load_3d(smem_u32(dst + b * C::kBoxBytes), map, b * 64, d.head, row, bar);
             }
           };
+          // VSA: a tile is two 64-row block boxes per 64-column half (block b0 in rows 0-63, b1 in
+          // rows 64-127; the 128-byte swizzle repeats every 8 rows, so the halves stack cleanly)
+          auto load_blocks = [&](uint8_t* dst, const CUtensorMap* map, int b0, int b1,
+                                 uint32_t bar) {
+            int t0, h0, w0;
+            for (int half = 0; half < 2; ++half) {
+              vsa_block_origin(half ? b1 : b0, wg, t0, h0, w0);
+              for (int b = 0; b < C::kBoxes; ++b)
+                tma_load_5d(smem_u32(dst + b * C::kBoxBytes + half * (C::kBoxBytes / 2)), map,
+                            b * 64, d.head, w0, h0, t0, bar);
+            }
+          };
           // Q tiles: after the previous item's last QK^T has read the buffers
           ok = mbar_wait(bar_qempty, (k & 1) ^ 1);
           if (!ok) break;
-          for (int t = 0; t < (has1 ? 2 : 1); ++t) {
-            mbar_arrive_expect_tx(bar_qfull(t), C::kTileBytes);
-            load_tile(sQ + t * C::kTileBytes, &tmap_q, t, d.q0 + t * kBlockM, bar_qfull(t));
-            ++qn[t];
-          }
-          for (int j = 0; j < nkv && ok; ++j) {
-            const int row = d.seg_start + j * kBlockN;
-            const int s = static_cast<int>(kt % SK);
-            ok = mbar_wait(bar_kempty(s), ((kt / SK) & 1) ^ 1);
-            if (!ok) break;
-            mbar_arrive_expect_tx(bar_kfull(s), C::kTileBytes);
-            load_tile(sK + s * C::kTileBytes, &tmap_k, j, row, bar_kfull(s));
-            ++kt;
-            const int v = static_cast<int>(vt % SV);
-            ok = mbar_wait(bar_vempty(v), ((vt / SV) & 1) ^ 1);
-            if (!ok) break;
-            mbar_arrive_expect_tx(bar_vfull(v), C::kTileBytes);
-            load_tile(sV + v * C::kTileBytes, &tmap_v, j, row, bar_vfull(v));
-            ++vt;
+          if constexpr (kVsa) {
+            // query blocks q0 .. q0 + 3 (a block past the last repeats the tile's first block:
+            // its rows are computed and never stored)
+            const int last = vsa_num_blocks(wg) - 1;
+            int qb[2][2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+              for (int h = 0; h < 2; ++h) qb[t][h] = min(d.q0 + 2 * t + h, last);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (t == 1 && !has1) break;
+              mbar_arrive_expect_tx(bar_qfull(t), C::kTileBytes);
+              load_blocks(sQ + t * C::kTileBytes, &tmap_q, qb[t][0], qb[t][1], bar_qfull(t));
+              ++qn[t];
+            }
+            // key/value steps: per step the K tiles of both query tiles, then their V tiles (the
+            // order in which the MMA warp consumes them); block ids are fetched one step ahead
+            int cur[2][2], nxt[2][2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                cur[t][h] = (t == 1 && !has1) ? 0 : vsa_selected(vsa_sel, d.head, qb[t][h], 0, wg, err);
+            for (int j = 0; j < nkv && ok; ++j) {
+#pragma unroll
+              for (int t = 0; t < 2; ++t)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                  nxt[t][h] = (j + 1 >= nkv || (t == 1 && !has1))
+                                  ? 0 : vsa_selected(vsa_sel, d.head, qb[t][h], j + 1, wg, err);
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                if (t == 1 && !has1) break;
+                const int s = static_cast<int>(kt % SK);
+                ok = mbar_wait(bar_kempty(s), ((kt / SK) & 1) ^ 1);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar_kfull(s), C::kTileBytes);
+                load_blocks(sK + s * C::kTileBytes, &tmap_k, cur[t][0], cur[t][1], bar_kfull(s));
+                ++kt;
+              }
+              if (!ok) break;
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                if (t == 1 && !has1) break;
+                const int v = static_cast<int>(vt % SV);
+                ok = mbar_wait(bar_vempty(v), ((vt / SV) & 1) ^ 1);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar_vfull(v), C::kTileBytes);
+                load_blocks(sV + v * C::kTileBytes, &tmap_v, cur[t][0], cur[t][1], bar_vfull(v));
+                ++vt;
+              }
+#pragma unroll
+              for (int t = 0; t < 2; ++t)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) cur[t][h] = nxt[t][h];
+            }
+          } else {
+            for (int t = 0; t < (has1 ? 2 : 1); ++t) {
+              mbar_arrive_expect_tx(bar_qfull(t), C::kTileBytes);
+              load_tile(sQ + t * C::kTileBytes, &tmap_q, t, d.q0 + t * kBlockM, bar_qfull(t));
+              ++qn[t];
+            }
+            for (int j = 0; j < nkv && ok; ++j) {
+              const int row = d.seg_start + j * kBlockN;
+              const int s = static_cast<int>(kt % SK);
+              ok = mbar_wait(bar_kempty(s), ((kt / SK) & 1) ^ 1);
+              if (!ok) break;
+              mbar_arrive_expect_tx(bar_kfull(s), C::kTileBytes);
+              load_tile(sK + s * C::kTileBytes, &tmap_k, j, row, bar_kfull(s));
+              ++kt;
+              const int v = static_cast<int>(vt % SV);
+              ok = mbar_wait(bar_vempty(v), ((vt / SV) & 1) ^ 1);
+              if (!ok) break;
+              mbar_arrive_expect_tx(bar_vfull(v), C::kTileBytes);
+              load_tile(sV + v * C::kTileBytes, &tmap_v, j, row, bar_vfull(v));
+              ++vt;
+            }
           }
         }
         if (!ok) record_error(err, kErrTimeout);
@@ -474,11 +614,60 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         __syncwarp();
         if (leader) mbar_arrive(bar_wempty(k & 1));
         if (d.seg_len < 0) break;
-        const ItemShape sh = shape_of<kWin>(d);
+        const ItemShape sh = shape_of<kMode>(d);
         const bool has1 = sh.has1;
         const int nkv = sh.nkv;
         const int kv_last_valid = sh.kv_last_valid;  // keys in the last tile (packed)
 
+        if constexpr (kVsa) {
+          // Each query tile has its own K/V stream: per step the rings hold K of tile 0, K of
+          // tile 1, then V of tile 0, V of tile 1.  Order per step j: PV0_j, S0_{j+1}, PV1_j,
+          // S1_{j+1}, as for shared tiles.
+          const int nt = has1 ? 2 : 1;
+          ok = wait_all(bar_qfull(0), qn[0]++ & 1);
+          if (ok && has1) ok = wait_all(bar_qfull(1), qn[1]++ & 1);
+          for (int t = 0; t < nt && ok; ++t) {
+            ok = wait_all(bar_kfull(kc % SK), (kc / SK) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            if (leader) {
+              issue_qk(t, kc % SK);
+              mma_commit(bar_kempty(kc % SK));
+              if (nkv == 1 && t == nt - 1) mma_commit(bar_qempty);
+            }
+            issued = true;
+            __syncwarp();
+            ++kc;
+          }
+          for (int j = 0; j < nkv && ok; ++j) {
+            const bool more = j + 1 < nkv;
+            for (int t = 0; t < nt; ++t) {
+              const int sv = static_cast<int>(vc % SV);
+              ok = wait_all(bar_vfull(sv), (vc / SV) & 1);
+              if (ok) ok = wait_all(bar_pfull(t), pn[t]++ & 1);
+              if (ok && j == 0) ok = wait_all(bar_oempty(t), (un[t] & 1) ^ 1);
+              if (ok && more) ok = wait_all(bar_kfull(kc % SK), (kc / SK) & 1);
+              if (!ok) break;
+              tc_fence_after();
+              if (leader) {
+                issue_pv(t, sv, j == 0);
+                mma_commit(bar_vempty(sv));
+                if (!more) mma_commit(bar_ofinal(t));
+                if (more) {
+                  issue_qk(t, kc % SK);
+                  mma_commit(bar_kempty(kc % SK));
+                  if (j + 2 == nkv && t == nt - 1) mma_commit(bar_qempty);
+                }
+              }
+              __syncwarp();
+              ++vc;
+              if (more) ++kc;
+            }
+          }
+          ++un[0];
+          if (has1) ++un[1];
+          continue;
+        }
         ok = wait_all(bar_qfull(0), qn[0]++ & 1);
         if (ok && has1) ok = wait_all(bar_qfull(1), qn[1]++ & 1);
         if (ok) ok = wait_all(bar_kfull(kc % SK), (kc / SK) & 1);
@@ -572,6 +761,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const uint32_t s_addr = tmem + lane_base + kColS + 128 * t;
     const uint32_t o_addr = tmem + lane_base + kColO + 128 * t;
     const float2 c2 = make_float2(scale_log2, scale_log2);
+    bool vsa_partial = false;  // VSA: some blocks are cropped by the grid edge (keys need masks)
+    if constexpr (kVsa)
+      vsa_partial = (wg.L[0] % wg.w[0]) != 0 || (wg.L[1] % wg.w[1]) != 0 || (wg.L[2] % wg.w[2]) != 0;
     uint32_t sn = 0, fn = 0;  // S groups and final-O completions seen by this tile slot
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -582,7 +774,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       if (lane == 0) mbar_arrive(bar_wempty(k & 1));
       if (d.seg_len < 0) break;
       const int seg_end = d.seg_start + d.seg_len;
-      const ItemShape sh = shape_of<kWin>(d);
+      const ItemShape sh = shape_of<kMode>(d);
       const bool has1 = sh.has1;
       if (t == 1 && !has1) continue;
       const int nkv = sh.nkv;
@@ -598,10 +790,90 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
       float m_used = -INFINITY;  // reference max (raw score units) used in the exponent
       float l = 0.f;
+      // New row max mx of step j: move the reference max (and rescale l and O_t) only when it
+      // grows by more than 2^kRescaleLog2.  O_t is stable when this runs: PV_t,{j-1} was issued
+      // before S_t,j, whose completion the caller observed.
+      auto update_max = [&](float mx, int j) {
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mx > m_used && (m_used == -INFINITY || (mx - m_used) * scale_log2 > kRescaleLog2)) {
+          alpha = ex2_approx((m_used - mx) * scale_log2);  // 0 when m_used == -inf
+          rescale = (j > 0);
+          l *= alpha;
+          m_used = mx;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t orr[32];
+            tmem_ld32(o_addr + c0, orr);
+            tmem_ld_wait();
+            tmem_reg_fence<32>(orr);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
+            tmem_st32(o_addr + c0, orr);
+          }
+        }
+      };
+      // VSA: this thread's half of the tile (warps 0-1 of the warpgroup: rows 0-63) is query
+      // block vqb; its keys fill the same half of every key tile, so it reads 64 columns of S
+      const int vhalf = (warp >> 1) & 1;
+      int vqb = 0;
+      if constexpr (kVsa) vqb = min(d.q0 + 2 * t + vhalf, vsa_num_blocks(wg) - 1);
       for (int j = 0; j < nkv; ++j) {
+        uint64_t vkm = ~0ull;  // VSA: rows of this step's key block that lie inside the grid
+        if constexpr (kVsa) {
+          if (vsa_partial) vkm = vsa_block_mask(vsa_selected(vsa_sel, d.head, vqb, j, wg, err), wg);
+        }
         ok = mbar_wait(bar_sfull(t), sn++ & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
+        if constexpr (kVsa) {
+          uint32_t sr[64];
+          tmem_ld32(s_addr + 64 * vhalf, sr);
+          tmem_ld32(s_addr + 64 * vhalf + 32, sr + 32);
+          tmem_ld_wait();
+          tmem_reg_fence<64>(sr);
+          float s[64];
+#pragma unroll
+          for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c]);
+          if (vkm != ~0ull) {
+            // key rows of an edge block outside the grid (zero-filled by TMA): -inf by select
+#pragma unroll
+            for (int c = 0; c < 64; ++c) s[c] = ((vkm >> c) & 1ull) ? s[c] : -INFINITY;
+          }
+          // row max over the 64 columns: four chains, 3-input steps over 4..59, then 60..63
+          float m4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+          for (int c = 4; c < 60; c += 8)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) m4[u] = fmax3(m4[u], s[c + u], s[c + 4 + u]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) m4[u] = fmaxf(m4[u], s[60 + u]);
+          update_max(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), j);
+          const float mb = m_used * scale_log2;
+          const float2 nm2 = make_float2(-mb, -mb);
+          float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+          uint32_t p[32], z[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), c2, nm2);
+            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            acc[c & 3] = fadd2(acc[c & 3], e);
+            p[c] = pack_bf16x2(e.x, e.y);
+            z[c] = 0u;
+          }
+          const float2 a01 = fadd2(acc[0], acc[1]);
+          const float2 a23 = fadd2(acc[2], acc[3]);
+          l += (a01.x + a01.y) + (a23.x + a23.y);
+          // P over S: this half's keys get P, the other block's keys weight 0 for these rows
+          tmem_st32(s_addr + 32 * vhalf, p);
+          tmem_st32(s_addr + 32 * (1 - vhalf), z);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar_pfull(t));
+          continue;
+        }
         uint32_t sr[128];
         tmem_ld32(s_addr + 0, sr + 0);
         tmem_ld32(s_addr + 32, sr + 32);
@@ -635,28 +907,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           for (int u = 0; u < 4; ++u) m4[u] = fmax3(m4[u], s[c + u], s[c + 4 + u]);
 #pragma unroll
         for (int u = 0; u < 4; ++u) m4[u] = fmaxf(m4[u], s[124 + u]);
-        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        float alpha = 1.f;
-        bool rescale = false;
-        if (mx > m_used && (m_used == -INFINITY || (mx - m_used) * scale_log2 > kRescaleLog2)) {
-          alpha = ex2_approx((m_used - mx) * scale_log2);  // 0 when m_used == -inf
-          rescale = (j > 0);
-          l *= alpha;
-          m_used = mx;
-        }
-        if (__any_sync(0xffffffffu, rescale)) {
-          // O_t is stable: PV_t,{j-1} was issued before S_t,j, whose completion we observed.
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t orr[32];
-            tmem_ld32(o_addr + c0, orr);
-            tmem_ld_wait();
-            tmem_reg_fence<32>(orr);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
-            tmem_st32(o_addr + c0, orr);
-          }
-        }
+        update_max(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), j);
         const float mb = m_used * scale_log2;
         const float2 nm2 = make_float2(-mb, -mb);
         float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
@@ -684,7 +935,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       tc_fence_after();
       int q_row;  // this thread's row in the output (original row-major order for windows)
       bool valid;
-      if constexpr (kWin) {
+      if constexpr (kVsa) {
+        // row r of the half = (ft * bh + fh) * bw + fw inside query block vqb
+        const int r64 = row & (kVsaBlockRows - 1);
+        int t0, h0, w0;
+        vsa_block_origin(vqb, wg, t0, h0, w0);
+        const int gt = t0 + r64 / (wg.w[1] * wg.w[2]);
+        const int gh = h0 + (r64 / wg.w[2]) % wg.w[1];
+        const int gw = w0 + r64 % wg.w[2];
+        valid = d.q0 + 2 * t + vhalf < vsa_num_blocks(wg) && gt < wg.L[0] && gh < wg.L[1] &&
+                gw < wg.L[2];
+        q_row = (gt * wg.L[1] + gh) * wg.L[2] + gw;
+      } else if constexpr (kWin) {
         const int pf = wg.w[1] * wg.w[2];
         const int gt = d.box[0] + t * wg.frames_per_tile + row / pf;
         const int gh = d.box[1] + (row / wg.w[2]) % wg.w[1];
@@ -748,7 +1010,7 @@ int num_sms_of_current_device() {
   return cached[dev];
 }
 
-template <int D, bool kWin>
+template <int D, int kMode>
 cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
   using C = Cfg<D>;
   static bool configured[64] = {};  // the shared-memory opt-in is made once per device
@@ -757,7 +1019,7 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D, kWin>,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, kMode>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
@@ -766,9 +1028,14 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
   if (sms <= 0) return cudaErrorInvalidDevice;
   uint32_t* ws = static_cast<uint32_t*>(a.workspace);
   long long max_items, want;
-  if (kWin) {
+  if (kMode == kModeWindow) {
     // windows hold at most 256 rows: one CTA per SM looping over (window, head) items
     max_items = static_cast<long long>(a.wg.nwin[0]) * a.wg.nwin[1] * a.wg.nwin[2] * a.num_heads;
+    want = sms;
+  } else if (kMode == kModeVsa) {
+    // four query blocks per item: one CTA per SM looping over (block quad, head) items
+    const long long nblk = static_cast<long long>(a.wg.nwin[0]) * a.wg.nwin[1] * a.wg.nwin[2];
+    max_items = (nblk + 3) / 4 * a.num_heads;
     want = sms;
   } else {
     attn_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.cu_seqlens, a.num_segments, a.capacity,
@@ -784,9 +1051,9 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
   if (max_items <= 0) return cudaSuccess;
   const int grid = static_cast<int>(max_items < want ? max_items : want);
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  attn_fwd_kernel<D, kWin><<<grid, kThreads, C::kSmemBytes, stream>>>(
+  attn_fwd_kernel<D, kMode><<<grid, kThreads, C::kSmemBytes, stream>>>(
       a.tmap_q, a.tmap_k, a.tmap_v, static_cast<__nv_bfloat16*>(a.o), a.lse, a.cu_seqlens,
-      a.num_segments, a.capacity, a.num_heads, a.scale, scale_log2, ws, a.wg, a.err);
+      a.num_segments, a.capacity, a.num_heads, a.scale, scale_log2, ws, a.wg, a.vsa_sel, a.err);
   return cudaGetLastError();
 }
 
@@ -798,13 +1065,17 @@ size_t attn_workspace_bytes(int num_segments) {
 }
 
 cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t stream) {
-  if (a.window) {
-    if (a.head_dim == 128) return launch<128, true>(a, stream);
-    return launch<64, true>(a, stream);
+  if (a.mode == kModeWindow) {
+    if (a.head_dim == 128) return launch<128, kModeWindow>(a, stream);
+    return launch<64, kModeWindow>(a, stream);
+  }
+  if (a.mode == kModeVsa) {
+    if (a.head_dim == 128) return launch<128, kModeVsa>(a, stream);
+    return launch<64, kModeVsa>(a, stream);
   }
   if (a.max_seqlen <= 0 || a.num_segments <= 0) return cudaSuccess;
-  if (a.head_dim == 128) return launch<128, false>(a, stream);
-  return launch<64, false>(a, stream);
+  if (a.head_dim == 128) return launch<128, kModePacked>(a, stream);
+  return launch<64, kModePacked>(a, stream);
 }
 
 }  // namespace h3

@@ -48,21 +48,32 @@ cudaError_t launch_window_unpack(const int32_t* perm, int num_tokens, const void
                                  int row_bytes, unsigned int* err, cudaStream_t stream);
 
 // ---- attention ------------------------------------------------------------------------------
-// Window attention straight on the (T, H, W) grid: windows of win[] cut with shift[] (edge
-// windows cropped), frames_per_tile = 128 / (win[1] * win[2]) frames of a window per 128-row tile.
+// Attention kernel variants: packed varlen segments; 3D windows read in place on the grid;
+// block-sparse video attention over selected 64-token blocks read in place on the grid.
+constexpr int kAttnModePacked = 0;
+constexpr int kAttnModeWindow = 1;
+constexpr int kAttnModeVsa = 2;
+
+// Attention straight on the (T, H, W) grid.
+// Windows: windows of w[] cut with shift s[] (edge windows cropped), nwin[] windows per axis,
+// frames_per_tile = 128 / (w[1] * w[2]) frames of a window per 128-row tile.
+// VSA: blocks of w[] (w[0] * w[1] * w[2] = 64) cut without shift (s = 0), nwin[] blocks per axis,
+// topk selected key blocks per query block.
 struct WindowAttnGeom {
   int L[3];
   int w[3];
   int s[3];
   int nwin[3];
   int frames_per_tile;
+  int topk;
 };
 
 struct AttnArgs {
   // packed: 3-D views {D, H, capacity} of Q, K, V; window: 5-D views {D, H, W, Hgrid, T}
   CUtensorMap tmap_q, tmap_k, tmap_v;
-  bool window;
+  int mode;            // kAttnModePacked / kAttnModeWindow / kAttnModeVsa
   WindowAttnGeom wg;
+  const int32_t* vsa_sel;  // VSA: [num_heads, nblk, topk] selected key blocks
   void* o;
   float* lse;
   const int32_t* cu_seqlens;
@@ -78,5 +89,18 @@ struct AttnArgs {
 
 size_t attn_workspace_bytes(int num_segments);
 cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t stream);
+
+// ---- VSA block gate + top-k ----------------------------------------------------------------
+struct VsaGeom {
+  int L[3];   // grid (T, H, W)
+  int b[3];   // block size per axis
+  int nb[3];  // blocks per axis = ceil(L / b)
+};
+// Workspace: block means of Q and K, fp32 [2][heads][nblk][head_dim].
+size_t vsa_pool_bytes(int nblk, int heads, int head_dim);
+// scores: fp32 [heads, nblk, nblk] out; sel: int32 [heads, nblk, topk] out (ascending ids).
+cudaError_t launch_vsa_select(const void* q, const void* k, const VsaGeom& g, int heads,
+                              int head_dim, int topk, float scale, float* scores, int32_t* sel,
+                              void* workspace, cudaStream_t stream);
 
 }  // namespace h3

@@ -151,6 +151,7 @@ const char* h3_status_string(h3_status s) {
     case H3_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
     case H3_ERR_MISALIGNED: return "a device pointer or row size is not 16-byte aligned";
     case H3_ERR_BAD_PERM: return "a permutation entry is out of range";
+    case H3_ERR_BAD_BLOCK_INDEX: return "a selected block index is out of range";
   }
   return "unknown status";
 }
@@ -343,7 +344,7 @@ h3_status h3_window_attn_fwd(const void* q, const void* k, const void* v, void* 
   if (!device_is_sm103()) return H3_ERR_UNSUPPORTED;
 
   h3::AttnArgs a{};
-  a.window = true;
+  a.mode = h3::kAttnModeWindow;
   const int frames = 128 / per_frame;
   for (int ax = 0; ax < 3; ++ax) {
     a.wg.L[ax] = grid[ax];
@@ -359,6 +360,121 @@ h3_status h3_window_attn_fwd(const void* q, const void* k, const void* v, void* 
   a.o = o;
   a.lse = lse;
   a.capacity = static_cast<int>(n);  // LSE row stride: [heads, T*H*W]
+  a.num_heads = num_heads;
+  a.head_dim = head_dim;
+  a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(head_dim));
+  a.err = device_error_ptr();
+  if (a.err == nullptr) return H3_ERR_CUDA;
+  return from_cuda(h3::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ---- VSA ----------------------------------------------------------------------------------------
+
+int32_t h3_vsa_block_count(const int32_t grid[3], const int32_t block[3]) {
+  if (grid == nullptr || block == nullptr) return -1;
+  int64_t n = 1;
+  for (int a = 0; a < 3; ++a) {
+    if (grid[a] <= 0 || block[a] <= 0) return -1;
+    n *= (static_cast<int64_t>(grid[a]) + block[a] - 1) / block[a];
+  }
+  return n > INT32_MAX ? -1 : static_cast<int32_t>(n);
+}
+
+namespace {
+
+// Shared checks of the VSA calls: a 64-token block (one half of a 128-row tile), a grid whose
+// rows and blocks fit the kernels' int32 indexing.
+h3_status vsa_geometry(const int32_t grid[3], const int32_t block[3], int32_t num_heads,
+                       int32_t head_dim, h3::VsaGeom* g) {
+  const int32_t nblk = h3_vsa_block_count(grid, block);
+  if (nblk < 0 || num_heads <= 0) return H3_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return H3_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(block[0]) * block[1] * block[2] != 64) return H3_ERR_UNSUPPORTED;
+  const int64_t n = static_cast<int64_t>(grid[0]) * grid[1] * grid[2];
+  if (n > INT32_MAX / 2 || static_cast<int64_t>(nblk) * num_heads > INT32_MAX / 4)
+    return H3_ERR_INVALID_ARG;
+  for (int a = 0; a < 3; ++a) {
+    g->L[a] = grid[a];
+    g->b[a] = block[a];
+    g->nb[a] = (grid[a] + block[a] - 1) / block[a];
+  }
+  return H3_OK;
+}
+
+}  // namespace
+
+size_t h3_vsa_select_workspace_size(const int32_t grid[3], const int32_t block[3],
+                                    int32_t num_heads, int32_t head_dim) {
+  h3::VsaGeom g;
+  if (vsa_geometry(grid, block, num_heads, head_dim, &g) != H3_OK) return 0;
+  return h3::vsa_pool_bytes(g.nb[0] * g.nb[1] * g.nb[2], num_heads, head_dim);
+}
+
+h3_status h3_vsa_select(const void* q, const void* k, const int32_t grid[3],
+                        const int32_t block[3], int32_t num_heads, int32_t head_dim,
+                        int32_t topk, float softmax_scale, float* scores, int32_t* block_idx,
+                        void* workspace, size_t workspace_bytes, h3_stream_t stream) {
+  if (q == nullptr || k == nullptr || grid == nullptr || block == nullptr || scores == nullptr ||
+      block_idx == nullptr)
+    return H3_ERR_NULL;
+  h3::VsaGeom g;
+  const h3_status st = vsa_geometry(grid, block, num_heads, head_dim, &g);
+  if (st != H3_OK) return st;
+  const int64_t nblk = static_cast<int64_t>(g.nb[0]) * g.nb[1] * g.nb[2];
+  if (topk < 1 || topk > nblk) return H3_ERR_INVALID_ARG;
+  if (nblk * nblk * num_heads > (static_cast<int64_t>(1) << 40)) return H3_ERR_INVALID_ARG;
+  if (!(softmax_scale <= 0.f || std::isfinite(softmax_scale))) return H3_ERR_INVALID_ARG;
+  if (workspace == nullptr ||
+      workspace_bytes < h3::vsa_pool_bytes(static_cast<int>(nblk), num_heads, head_dim))
+    return H3_ERR_WORKSPACE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(scores) & 3u) || (reinterpret_cast<uintptr_t>(block_idx) & 3u))
+    return H3_ERR_MISALIGNED;
+  if (!device_is_sm103()) return H3_ERR_UNSUPPORTED;
+  const float scale =
+      softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(head_dim));
+  return from_cuda(h3::launch_vsa_select(q, k, g, num_heads, head_dim, topk, scale, scores,
+                                         block_idx, workspace,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+h3_status h3_vsa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int32_t grid[3], const int32_t block[3], int32_t num_heads,
+                          int32_t head_dim, const int32_t* block_idx, int32_t topk,
+                          float softmax_scale, h3_stream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || grid == nullptr ||
+      block == nullptr || block_idx == nullptr)
+    return H3_ERR_NULL;
+  h3::VsaGeom g;
+  const h3_status st = vsa_geometry(grid, block, num_heads, head_dim, &g);
+  if (st != H3_OK) return st;
+  const int64_t nblk = static_cast<int64_t>(g.nb[0]) * g.nb[1] * g.nb[2];
+  if (topk < 1 || topk > nblk) return H3_ERR_INVALID_ARG;
+  if (!(softmax_scale <= 0.f || std::isfinite(softmax_scale))) return H3_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
+      (reinterpret_cast<uintptr_t>(block_idx) & 3u))
+    return H3_ERR_MISALIGNED;
+  if (!device_is_sm103()) return H3_ERR_UNSUPPORTED;
+
+  h3::AttnArgs a{};
+  a.mode = h3::kAttnModeVsa;
+  for (int ax = 0; ax < 3; ++ax) {
+    a.wg.L[ax] = grid[ax];
+    a.wg.w[ax] = block[ax];
+    a.wg.s[ax] = 0;
+    a.wg.nwin[ax] = g.nb[ax];
+  }
+  a.wg.topk = topk;
+  a.vsa_sel = block_idx;
+  // one block (bw x bh x bt = 64 rows) per box
+  if (!make_window_map(&a.tmap_q, q, grid, block, block[0], num_heads, head_dim) ||
+      !make_window_map(&a.tmap_k, k, grid, block, block[0], num_heads, head_dim) ||
+      !make_window_map(&a.tmap_v, v, grid, block, block[0], num_heads, head_dim))
+    return H3_ERR_CUDA;
+  a.o = o;
+  a.lse = lse;
+  a.capacity = grid[0] * grid[1] * grid[2];  // LSE row stride: [heads, T*H*W]
   a.num_heads = num_heads;
   a.head_dim = head_dim;
   a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(head_dim));

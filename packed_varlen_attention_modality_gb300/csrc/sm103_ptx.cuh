@@ -15,6 +15,7 @@ enum : unsigned int {
   kErrBadCuSeqlens = 3,
   kErrTimeout = 7,
   kErrBadPerm = 9,
+  kErrBadBlockIndex = 10,
 };
 
 // Longest legitimate wait inside one kernel is microseconds; give up after 2 s.

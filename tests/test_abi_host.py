@@ -58,7 +58,7 @@ def test_workspace_size_grows_with_segments(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.h3_version() == 100
-    for s in range(10):
+    for s in range(11):
         assert len(lib.h3_status_string(s)) >= 2
     assert lib.h3_status_string(99) == b"unknown status"
 
@@ -155,3 +155,42 @@ def test_window_attention_rejects_bad_arguments_on_the_host(lib):
     assert call(win=_i3((4, 8, 12))) == 4   # 8*12 does not divide 128
     assert call(win=_i3((8, 8, 8))) == 4    # 512 rows: more than two 128-row tiles
     assert call(q=FAKE + 8) == 8
+
+
+@pytest.mark.parametrize("grid,block", [((29, 40, 50), (4, 4, 4)), ((32, 48, 84), (4, 4, 4)),
+                                        ((5, 9, 11), (2, 4, 8)), ((1, 1, 1), (4, 4, 4))])
+def test_vsa_block_count_matches_oracle(lib, grid, block):
+    assert lib.h3_vsa_block_count(_i3(grid), _i3(block)) == oracle.vsa_block_count(grid, block)
+    assert lib.h3_vsa_block_count(_i3((0, 4, 4)), _i3(block)) == -1
+
+
+def test_vsa_workspace_size_holds_both_block_means(lib):
+    ws = lib.h3_vsa_select_workspace_size(_i3((32, 48, 84)), _i3((4, 4, 4)), 24, 128)
+    assert ws % 256 == 0 and ws >= 2 * 24 * 2016 * 128 * 4
+    assert lib.h3_vsa_select_workspace_size(_i3((32, 48, 84)), _i3((4, 4, 8)), 24, 128) == 0  # 128-token block
+    assert lib.h3_vsa_select_workspace_size(_i3((32, 48, 84)), _i3((4, 4, 4)), 24, 96) == 0
+
+
+def test_vsa_calls_reject_bad_arguments_on_the_host(lib):
+    P = ctypes.c_void_p
+    g, b = _i3((8, 8, 8)), _i3((4, 4, 4))   # 8 blocks
+    ws = lib.h3_vsa_select_workspace_size(g, b, 2, 128)
+
+    def sel(q=FAKE, topk=3, D=128, block=b, wsb=ws, w=FAKE, scores=FAKE):
+        return lib.h3_vsa_select(P(q) if q else None, P(FAKE), g, block, 2, D, topk, 0.0,
+                                 P(scores) if scores else None, P(FAKE), P(w) if w else None, wsb, None)
+
+    assert sel(q=0) == 1 and sel(scores=0) == 1
+    assert sel(topk=0) == 2 and sel(topk=9) == 2
+    assert sel(D=96) == 4 and sel(block=_i3((4, 4, 8))) == 4
+    assert sel(w=0) == 5 and sel(wsb=ws - 1) == 5
+    assert sel(q=FAKE + 8) == 8 and sel(scores=FAKE + 2) == 8
+
+    def attn(q=FAKE, topk=3, D=128, block=b, idx=FAKE):
+        return lib.h3_vsa_attn_fwd(P(q) if q else None, P(FAKE), P(FAKE), P(FAKE), None, g, block, 2, D,
+                                   P(idx) if idx else None, topk, 0.0, None)
+
+    assert attn(q=0) == 1 and attn(idx=0) == 1
+    assert attn(topk=0) == 2 and attn(topk=9) == 2
+    assert attn(D=64, block=_i3((2, 2, 2))) == 4
+    assert attn(q=FAKE + 8) == 8 and attn(idx=FAKE + 2) == 8

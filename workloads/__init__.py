@@ -13,7 +13,9 @@ Shapes follow the pages:
   * the cu_seqlens worked example [0,10,30,45] (same page, section 3, "minimal example");
   * continuation requests whose time axis is shifted by the start frame s
     ("MiniMax H3 fast and strong", continuation, step 3 "RoPE global time alignment");
-  * a 3D latent grid cut into (shifted) windows (same page, "window-aligned SP").
+  * a 3D latent grid cut into (shifted) windows (same page, "window-aligned SP");
+  * the same grid attended block-sparsely over 4x4x4 blocks (same page, "VSA"); the pages give
+    no top-k ratio, the default keeps 1/8 of the blocks.
 
 Modality tags: 0 = text, 1 = video, 2 = audio.
 """
@@ -251,6 +253,43 @@ def video_segment_16k(seed: int = 6) -> PackedWorkload:
     return _assemble("video_segment_16384tok_40x128", seed, 40, 128, parts, [0, 16384], [0.0], None)
 
 
+@dataclass
+class VsaWorkload:
+    """A 3D latent grid (T, H, W) in row-major token order, attended over selected blocks."""
+
+    name: str
+    num_heads: int
+    head_dim: int
+    grid: Tuple[int, int, int]
+    block: Tuple[int, int, int]
+    topk: int
+    q: torch.Tensor  # bf16 [N, H, D]
+    k: torch.Tensor
+    v: torch.Tensor
+
+    @property
+    def num_tokens(self) -> int:
+        t, h, w = self.grid
+        return t * h * w
+
+
+def vsa_video(seed: int = 7, grid=(32, 48, 84), block=(4, 4, 4), heads: int = 24,
+              head_dim: int = 128, topk: Optional[int] = None) -> VsaWorkload:
+    """Q/K/V ~ N(0,1) in bf16 over a (T, H, W) latent grid; 32x48x84 is the latent of a
+    1344x768 video (16x spatial compression), the resolution the pages quote for VSA.  topk
+    defaults to 1/8 of the blocks (rounded down, at least 1)."""
+    rng = np.random.default_rng(seed)
+    n = grid[0] * grid[1] * grid[2]
+    nblk = 1
+    for L, b in zip(grid, block):
+        nblk *= (L + b - 1) // b
+    k_sel = max(1, nblk // 8) if topk is None else int(topk)
+    q, k, v = (_normal_bf16(rng, (n, heads, head_dim)) for _ in range(3))
+    return VsaWorkload(name=f"vsa_{grid[0]}x{grid[1]}x{grid[2]}_b{block[0]}x{block[1]}x{block[2]}_top{k_sel}",
+                       num_heads=heads, head_dim=head_dim, grid=tuple(grid), block=tuple(block),
+                       topk=k_sel, q=q, k=k, v=v)
+
+
 WORKLOADS = {
     "tiny_example": tiny_example,
     "single_request_4k": single_request_4k,
@@ -258,4 +297,5 @@ WORKLOADS = {
     "continuation_batch": continuation_batch,
     "window_grid": window_grid,
     "video_segment_16k": video_segment_16k,
+    "vsa_video": vsa_video,
 }
