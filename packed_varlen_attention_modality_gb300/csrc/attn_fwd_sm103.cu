@@ -46,6 +46,8 @@
 // wait's parity from them; no waiter can fall more than one phase behind its barrier.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "h3_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -191,13 +193,17 @@ __device__ __forceinline__ uint64_t vsa_block_mask(int b, const WindowAttnGeom& 
   return m;
 }
 // Item -> descriptor: query blocks q0 .. q0 + 3 of one head (tile t holds blocks q0 + 2t and
-// q0 + 2t + 1 in its two 64-row halves), head fastest.
+// q0 + 2t + 1 in its two 64-row halves).  Items are numbered head-major: the CTAs working at one
+// time serve one head (two at a boundary), so the key/value blocks they select at random stay
+// in L2 (one head's K and V of the 32x48x84 grid are 66 MB), instead of every head's at once.
 __device__ __forceinline__ WorkDesc decode_vsa(uint32_t item, const WindowAttnGeom& g,
                                                int num_heads) {
   WorkDesc d{};
   d.seg_len = 1;
-  d.head = static_cast<int>(item % static_cast<uint32_t>(num_heads));
-  d.q0 = 4 * static_cast<int>(item / static_cast<uint32_t>(num_heads));
+  const uint32_t quads = static_cast<uint32_t>((vsa_num_blocks(g) + 3) / 4);
+  d.head = static_cast<int>(item / quads);
+  d.q0 = 4 * static_cast<int>(item % quads);
+  (void)num_heads;
   d.ntiles = d.q0 + 2 < vsa_num_blocks(g) ? 2 : 1;
   d.nkv = g.topk;
   return d;
@@ -306,13 +312,17 @@ __device__ __forceinline__ WorkDesc decode_item(uint32_t item, const uint32_t* _
   return d;
 }
 
-template <int D>
+template <int D, int kMode>
 struct Cfg {
   static constexpr int kBoxes = D / 64;               // 64-column (128-byte) swizzle boxes
   static constexpr int kTileBytes = kBlockM * D * 2;  // one Q, K or V tile
   static constexpr int kBoxBytes = kBlockM * 128;     // one 128-row box
-  static constexpr int kStagesK = (D == 128) ? 3 : 4;  // K ring depth
-  static constexpr int kStagesV = (D == 128) ? 2 : 4;  // V ring depth
+  // Ring depths (5 tiles of 32 KB fit beside the two Q tiles at D = 128).  Shared key/value
+  // tiles: 3 K + 2 V.  VSA, where every step takes a K and a V tile per query tile: 2 K + 3 V
+  // (a V tile is loaded only once the PV product two entries back has drained, so V needs the
+  // deeper ring; measured 50 -> 39 ms on the 1344x768 latent).
+  static constexpr int kStagesK = (D == 128) ? (kMode == kModeVsa ? 2 : 3) : 4;
+  static constexpr int kStagesV = (D == 128) ? (kMode == kModeVsa ? 3 : 2) : 4;
   // q_full[2], q_empty, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
   // p_full[2], o_final[2], o_empty[2], w_full[2], w_empty[2], drain
   static constexpr int kNumBars = 3 + 2 * kStagesK + 2 * kStagesV + 12 + 1;
@@ -322,6 +332,34 @@ struct Cfg {
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(kBlockM, kBlockN, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, true);
 };
+
+// VSA: the query blocks of an item's tiles, qb[t][half] (a block past the last repeats the
+// tile's first block: its rows are computed and never stored).
+__device__ __forceinline__ void vsa_item_blocks(const WorkDesc& d, const WindowAttnGeom& g,
+                                                int (&qb)[2][2]) {
+  const int last = vsa_num_blocks(g) - 1;
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) qb[t][h] = min(d.q0 + 2 * t + h, last);
+}
+
+// VSA: one 128-row tile from two blocks' 64-row boxes (block b0 in rows 0-63, b1 in rows 64-127
+// of every 64-column half; the 128-byte swizzle repeats every 8 rows, so the halves stack).
+template <int kBoxes, int kBoxBytes>
+__device__ __forceinline__ void vsa_load_tile(uint8_t* dst, const CUtensorMap* map, int head,
+                                              int b0, int b1, uint32_t bar,
+                                              const WindowAttnGeom& g) {
+  int t0, h0, w0;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    vsa_block_origin(half ? b1 : b0, g, t0, h0, w0);
+#pragma unroll
+    for (int b = 0; b < kBoxes; ++b)
+      tma_load_5d(smem_u32(dst + b * kBoxBytes + half * (kBoxBytes / 2)), map, b * 64, head, w0,
+                  h0, t0, bar);
+  }
+}
 
 // kModePacked: packed varlen segments (cu_seqlens, 3-D tensor maps, rows of [capacity, H, D]).
 // kModeWindow: windows of a (T, H, W) grid read in place (5-D tensor maps over [T, H, W, heads, D]
@@ -340,7 +378,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 const int32_t* __restrict__ vsa_sel, unsigned int* err) {
   constexpr bool kWin = kMode == kModeWindow;
   constexpr bool kVsa = kMode == kModeVsa;
-  using C = Cfg<D>;
+  using C = Cfg<D, kMode>;
   constexpr int SK = C::kStagesK;
   constexpr int SV = C::kStagesV;
   extern __shared__ uint8_t smem_raw[];
@@ -387,7 +425,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       mbar_init(bar_ofinal(t), 1);
       mbar_init(bar_oempty(t), 128);
       mbar_init(bar_wfull(t), 1);
-      mbar_init(bar_wempty(t), 9);  // the MMA warp + lane 0 of each of the 8 softmax warps
+      // the MMA warp + lane 0 of each of the 8 softmax warps (+ the VSA value producer)
+      mbar_init(bar_wempty(t), kVsa ? 10 : 9);
     }
     mbar_init(bar_qempty, 1);
     for (int s = 0; s < SK; ++s) {
@@ -409,6 +448,46 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // VSA: stream an item's selected key (or value) blocks through one ring, per step the tile of
+  // query tile 0 then of tile 1 (the order the MMA warp consumes them); block ids are fetched one
+  // step ahead.  K and V have a producer thread each (warps 8 and 10), so a wait on one ring never
+  // holds back loads for the other.  Returns false when a wait ran out.
+  auto vsa_stream = [&](const WorkDesc& d, auto stages, uint8_t* ring, const CUtensorMap* map,
+                        uint32_t full0, uint32_t empty0, uint32_t& cnt) -> bool {
+    constexpr int S = decltype(stages)::value;
+    const bool has1 = d.ntiles == 2;
+    int qb[2][2], cur[2][2], nxt[2][2];
+    vsa_item_blocks(d, wg, qb);
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        cur[t][h] = (t == 1 && !has1) ? 0 : vsa_selected(vsa_sel, d.head, qb[t][h], 0, wg, err);
+    for (int j = 0; j < d.nkv; ++j) {
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          nxt[t][h] = (j + 1 >= d.nkv || (t == 1 && !has1))
+                          ? 0 : vsa_selected(vsa_sel, d.head, qb[t][h], j + 1, wg, err);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (t == 1 && !has1) break;
+        const uint32_t s = cnt % S;
+        if (!mbar_wait(empty0 + 8 * s, ((cnt / S) & 1) ^ 1)) return false;
+        mbar_arrive_expect_tx(full0 + 8 * s, C::kTileBytes);
+        vsa_load_tile<C::kBoxes, C::kBoxBytes>(ring + s * C::kTileBytes, map, d.head, cur[t][0],
+                                               cur[t][1], full0 + 8 * s, wg);
+        ++cnt;
+      }
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) cur[t][h] = nxt[t][h];
+    }
+    return true;
+  };
 
   if (warp >= 8) {
     setmaxnreg_dec<kRegsOther>();
@@ -460,78 +539,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 tma_load_3d(smem_u32(dst + b * C::kBoxBytes), map, b * 64, d.head, row, bar);
             }
           };
-          // VSA: a tile is two 64-row block boxes per 64-column half (block b0 in rows 0-63, b1 in
-          // rows 64-127; the 128-byte swizzle repeats every 8 rows, so the halves stack cleanly)
-          auto load_blocks = [&](uint8_t* dst, const CUtensorMap* map, int b0, int b1,
-                                 uint32_t bar) {
-            int t0, h0, w0;
-            for (int half = 0; half < 2; ++half) {
-              vsa_block_origin(half ? b1 : b0, wg, t0, h0, w0);
-              for (int b = 0; b < C::kBoxes; ++b)
-                tma_load_5d(smem_u32(dst + b * C::kBoxBytes + half * (C::kBoxBytes / 2)), map,
-                            b * 64, d.head, w0, h0, t0, bar);
-            }
-          };
           // Q tiles: after the previous item's last QK^T has read the buffers
           ok = mbar_wait(bar_qempty, (k & 1) ^ 1);
           if (!ok) break;
           if constexpr (kVsa) {
-            // query blocks q0 .. q0 + 3 (a block past the last repeats the tile's first block:
-            // its rows are computed and never stored)
-            const int last = vsa_num_blocks(wg) - 1;
             int qb[2][2];
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-#pragma unroll
-              for (int h = 0; h < 2; ++h) qb[t][h] = min(d.q0 + 2 * t + h, last);
+            vsa_item_blocks(d, wg, qb);
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
               if (t == 1 && !has1) break;
               mbar_arrive_expect_tx(bar_qfull(t), C::kTileBytes);
-              load_blocks(sQ + t * C::kTileBytes, &tmap_q, qb[t][0], qb[t][1], bar_qfull(t));
+              vsa_load_tile<C::kBoxes, C::kBoxBytes>(sQ + t * C::kTileBytes, &tmap_q, d.head,
+                                                     qb[t][0], qb[t][1], bar_qfull(t), wg);
               ++qn[t];
             }
-            // key/value steps: per step the K tiles of both query tiles, then their V tiles (the
-            // order in which the MMA warp consumes them); block ids are fetched one step ahead
-            int cur[2][2], nxt[2][2];
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-                cur[t][h] = (t == 1 && !has1) ? 0 : vsa_selected(vsa_sel, d.head, qb[t][h], 0, wg, err);
-            for (int j = 0; j < nkv && ok; ++j) {
-#pragma unroll
-              for (int t = 0; t < 2; ++t)
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                  nxt[t][h] = (j + 1 >= nkv || (t == 1 && !has1))
-                                  ? 0 : vsa_selected(vsa_sel, d.head, qb[t][h], j + 1, wg, err);
-#pragma unroll
-              for (int t = 0; t < 2; ++t) {
-                if (t == 1 && !has1) break;
-                const int s = static_cast<int>(kt % SK);
-                ok = mbar_wait(bar_kempty(s), ((kt / SK) & 1) ^ 1);
-                if (!ok) break;
-                mbar_arrive_expect_tx(bar_kfull(s), C::kTileBytes);
-                load_blocks(sK + s * C::kTileBytes, &tmap_k, cur[t][0], cur[t][1], bar_kfull(s));
-                ++kt;
-              }
-              if (!ok) break;
-#pragma unroll
-              for (int t = 0; t < 2; ++t) {
-                if (t == 1 && !has1) break;
-                const int v = static_cast<int>(vt % SV);
-                ok = mbar_wait(bar_vempty(v), ((vt / SV) & 1) ^ 1);
-                if (!ok) break;
-                mbar_arrive_expect_tx(bar_vfull(v), C::kTileBytes);
-                load_blocks(sV + v * C::kTileBytes, &tmap_v, cur[t][0], cur[t][1], bar_vfull(v));
-                ++vt;
-              }
-#pragma unroll
-              for (int t = 0; t < 2; ++t)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) cur[t][h] = nxt[t][h];
-            }
+            ok = vsa_stream(d, std::integral_constant<int, SK>{}, sK, &tmap_k, bar_kfull(0),
+                            bar_kempty(0), kt);
           } else {
             for (int t = 0; t < (has1 ? 2 : 1); ++t) {
               mbar_arrive_expect_tx(bar_qfull(t), C::kTileBytes);
@@ -751,6 +774,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         mbar_wait(bar_drain, 0);
       }
       __syncwarp();
+    } else if (kVsa && warp == 10) {
+      // ================= VSA value producer =================
+      if (lane == 0) {
+        uint32_t vt = 0;  // V tiles loaded so far
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+          ok = mbar_wait(bar_wfull(k & 1), (k >> 1) & 1);
+          if (!ok) break;
+          const WorkDesc d = work[k & 1];
+          mbar_arrive(bar_wempty(k & 1));
+          if (d.seg_len < 0) break;
+          ok = vsa_stream(d, std::integral_constant<int, SV>{}, sV, &tmap_v, bar_vfull(0),
+                          bar_vempty(0), vt);
+        }
+        if (!ok) record_error(err, kErrTimeout);
+        for (uint32_t i = 0; i < SV && i < vt; ++i) {  // drain, as for the other producer
+          const uint32_t x = vt - 1 - i;
+          mbar_wait(bar_vfull(x % SV), (x / SV) & 1);
+        }
+      }
     }
   } else {
     setmaxnreg_inc<kRegsSoftmax>();
@@ -1012,7 +1055,7 @@ int num_sms_of_current_device() {
 
 template <int D, int kMode>
 cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kMode>;
   static bool configured[64] = {};  // the shared-memory opt-in is made once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
