@@ -17,7 +17,9 @@ Sources (page title + section):
              "Breaking the memory wall: window attention across GPUs" (regular and half-shifted
              3D windows, edge windows cropped, token order restored afterwards);
              "VSA: block-sparse attention" (64-token 4x4x4 blocks, block-level gated scoring,
-             top-k block selection, token-level attention between the selected blocks).
+             top-k block selection, token-level attention between the selected blocks);
+             "Crossing the time boundary", steps 1-2 and the overlap discard (7-frame video tail,
+             40 Hz audio tail, five row groups, target-only updates, suffix append).
 
 Every function here is pinned by tests/test_oracle_pins.py against closed forms, textbook
 routines, brute force and the pages' printed examples.  Readings where the pages are silent
@@ -28,6 +30,8 @@ from .rope import (continuation_time_shift, rope_inv_freq, rope_angles, rope_app
                    video_axis_split)
 from .window import (axis_window_count, window_count, window_ids, window_partition,
                      window_pack, window_unpack)
+from .continuation import (ContinuationPlan, continuation_plan, continuation_pack,
+                           continuation_append, masked_update)
 from .vsa import (vsa_block_counts, vsa_block_count, vsa_block_ids, vsa_block_means,
                   vsa_block_scores, vsa_select, vsa_attention)
 
@@ -36,5 +40,6 @@ __all__ = [
     "continuation_time_shift", "rope_inv_freq", "rope_angles", "rope_apply", "video_axis_split",
     "axis_window_count", "window_count", "window_ids", "window_partition", "window_pack",
     "window_unpack", "vsa_block_counts", "vsa_block_count", "vsa_block_ids", "vsa_block_means",
-    "vsa_block_scores", "vsa_select", "vsa_attention",
+    "vsa_block_scores", "vsa_select", "vsa_attention", "ContinuationPlan", "continuation_plan",
+    "continuation_pack", "continuation_append", "masked_update",
 ]
