@@ -44,7 +44,7 @@ def parse_args():
     p.add_argument("--workload", default="h3_full_request",
                    choices=["h3_full_request", "single_request_4k", "continuation_batch",
                             "video_segment_16k", "window_grid", "window_grid_16x24x84",
-                            "vsa_video", "vsa_video_16x24x84"],
+                            "vsa_video", "vsa_video_16x24x84", "continuation_window"],
                    help="h3_full_request is the metric's workload; the others are side measurements")
     return p.parse_args()
 
@@ -229,6 +229,8 @@ def run_ours(args, rank, world, local_rank):
         return run_window(args, rank, world, dev, h3, peaks)
     if args.workload.startswith("vsa_video"):
         return run_vsa(args, rank, world, dev, h3, peaks)
+    if args.workload == "continuation_window":
+        return run_continuation(args, rank, world, dev, h3, peaks)
     headline = args.workload == "h3_full_request"
     wl = workloads.WORKLOADS[args.workload]()
     H, D, C, N = wl.num_heads, wl.head_dim, wl.capacity, wl.num_tokens
@@ -609,6 +611,91 @@ def run_vsa(args, rank, world, dev, h3, peaks):
                          "peak_source": peaks["source"] + " bf16_tflops (burst)",
                          "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"]},
             "clocks": clocks, "gpu_launches": 4 * args.steps}), flush=True)
+
+
+def run_continuation(args, rank, world, dev, h3, peaks):
+    """Continuation window around the H3 request shape: the clip so far is one 5 s window (29
+    latent frames of 40x50, 200 audio rows at 40 Hz), the next window has the same shape, rows are
+    40 heads x 128 bf16 (10 KB).  Per step: pack the five row groups (+ positions, tags, target
+    mask), one target-only row update over the packed sequence, append the new rows past the
+    overlap to the clip."""
+    H, D = 40, 128
+    text, cf, ca, fh, fw, nf, na = 558, 29, 200, 40, 50, 29, 200
+    cfg = h3.continuation_config(text, cf, ca, fh, fw, nf, na)
+    plan = h3.continuation_plan(cfg)
+    hw = fh * fw
+    gen = torch.Generator(device=dev).manual_seed(8)
+    mk = lambda n: torch.randn((n, H, D), generator=gen, device=dev).to(torch.bfloat16)
+    t_rows, new_v, new_a = mk(text), mk(nf * hw), mk(na)
+    clip_v = mk(plan.out_video_frames * hw)   # room for the append
+    clip_a = mk(plan.out_audio_rows)
+    n = plan.num_rows
+    rows = torch.empty((n, H, D), dtype=torch.bfloat16, device=dev)
+    upd = mk(n)
+    row_bytes = H * D * 2
+    stream = torch.cuda.current_stream(dev)
+    # the clip's first cf frames / ca rows are its content; pack reads the tail from them
+    src = dict(text=t_rows, clip_video=clip_v[:cf * hw], clip_audio=clip_a[:ca], new_video=new_v,
+               new_audio=new_a)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        _, pos, tag, target = h3.continuation_pack(cfg, src["text"], src["clip_video"], src["clip_audio"],
+                                                   src["new_video"], src["new_audio"], out=rows)
+        if ev is not None:
+            ev[1].record(stream)
+        h3.masked_row_update(rows, upd, target)
+        if ev is not None:
+            ev[2].record(stream)
+        h3.continuation_append(cfg, new_v, new_a, clip_v, clip_a)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if h3.get_device_error(dev) != 0:
+        raise RuntimeError("device error during the timed steps")
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, world, dev)
+    n_tgt = n - plan.group_offset[3]
+    pack_bytes = 2.0 * n * row_bytes + 14.0 * n              # rows in + out; pos 12 B, tag, target
+    upd_bytes = 2.0 * n_tgt * row_bytes + n                   # target rows read + written; the mask
+    app_rows = (nf - plan.keep_video_from) * hw + (na - plan.keep_audio_from)
+    app_bytes = 2.0 * app_rows * row_bytes
+    per = {}
+    for name, a, b, nbytes in (("pack", 0, 1, pack_bytes), ("masked_update", 1, 2, upd_bytes),
+                               ("append", 2, 3, app_bytes)):
+        t = float(np.mean([e[a].elapsed_time(e[b]) for e in evs]))
+        per[name] = {"ms": t, "bytes": nbytes, "gbs": nbytes / t / 1e6, "frac_hbm": nbytes / t / 1e6 / peaks["hbm_gbs"]}
+    total_bytes = pack_bytes + upd_bytes + app_bytes
+    if rank == 0:
+        achieved = per["pack"]["gbs"]
+        print(json.dumps({
+            "metric": "continuation window GB/s (pack + target-only update + append)",
+            "value": world * total_bytes / ms / 1e6, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "continuation_h3_window_29x40x50_a200", "packed_rows": n,
+                       "row_bytes": row_bytes, "start_frame": plan.start_frame, "audio_cut": plan.audio_cut,
+                       "l2": "inputs larger than L2 (%.0f MB packed)" % (n * row_bytes / 1e6)},
+            "kernels": per,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "kernel": "continuation_pack_kernel",
+                         "peak_source": "%s (copy bandwidth)" % peaks["source"]},
+            "clocks": clocks, "gpu_launches": 3 * args.steps}), flush=True)
 
 
 def _block_sizes(grid, block):

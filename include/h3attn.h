@@ -286,6 +286,80 @@ H3_API h3_status h3_vsa_attn_fwd(const void* q, const void* k, const void* v, vo
                                  int32_t head_dim, const int32_t* block_idx, int32_t topk,
                                  float softmax_scale, h3_stream_t stream);
 
+/* ---- Continuation window ---------------------------------------------------------------------
+ * [H3-fast] "Breaking the engineering bottlenecks of video-generation models", section "Crossing
+ * the time boundary": the last 7 latent video frames and the audio tail cut on the global 40 Hz
+ * boundary are taken from the previous window's latents (step 1); the DiT sequence concatenates
+ * (1) text / reference rows, (2) the audio tail, (3) the video tail, (4) new audio noise,
+ * (5) new video noise, and only (4) and (5) are updated by the denoising steps (step 2); every
+ * row's time coordinate is shifted by s * 40 / 24 before RoPE (step 3, h3_rope_apply with
+ * start_frames = {s}); afterwards the new samples overlapping the tails are discarded and the
+ * rest is appended to the clip.
+ *
+ * Readings where the pages leave a step open: a latent frame spans frames_per_latent video frames
+ * at 24 FPS and audio latents are 40 Hz rows; the new window starts where the video tail starts,
+ * g0 = clip_video_frames - tail_frames latent frames, s = g0 * frames_per_latent; the audio tail
+ * starts at row floor(s * 40 / 24) (the row holding time s / 24 s); positions are local to the new
+ * window (the tails and the new rows both start at t = 0); every group shares one row size; the
+ * whole sequence is one attention segment.  Rows of every tensor are row_bytes bytes, contiguous;
+ * video latents are frames of frame_h x frame_w rows in row-major (t, h, w) order. */
+typedef struct {
+  int32_t text_rows;           /* group 1 */
+  int32_t clip_video_frames;   /* latent frames in the clip so far (>= tail_frames) */
+  int32_t clip_audio_rows;     /* 40 Hz audio rows in the clip so far */
+  int32_t frame_h, frame_w;    /* latent grid of one video frame */
+  int32_t new_video_frames;    /* latent frames the new window samples (>= tail_frames) */
+  int32_t new_audio_rows;      /* audio rows the new window samples (>= the audio tail) */
+  int32_t tail_frames;         /* video tail, 7 on the pages */
+  int32_t frames_per_latent;   /* video frames (24 FPS) per latent frame */
+} h3_continuation_cfg;
+
+typedef struct {
+  int32_t tail_start;          /* g0: first latent frame of the video tail */
+  int32_t start_frame;         /* s = g0 * frames_per_latent (the RoPE start frame) */
+  int32_t audio_cut;           /* first audio row of the audio tail, min(floor(s*40/24), clip rows) */
+  int32_t group_rows[5];       /* rows of the five groups in packed order */
+  int32_t group_offset[6];     /* exclusive prefix of group_rows */
+  int32_t num_rows;            /* rows of the packed sequence */
+  int32_t keep_video_from;     /* first new latent frame appended (= tail_frames) */
+  int32_t keep_audio_from;     /* first new audio row appended (= clip_audio_rows - audio_cut) */
+  int32_t out_video_frames;    /* clip length after the append */
+  int32_t out_audio_rows;
+} h3_continuation_plan;
+
+/* Host-only index math of a continuation window (no device work).
+ * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG (a negative size, a clip or new window shorter than the
+ * tail, new audio shorter than the audio tail, more than INT32_MAX rows). */
+H3_API h3_status h3_continuation_make_plan(const h3_continuation_cfg* cfg, h3_continuation_plan* plan);
+
+/* Pack the five groups: rows [num_rows, row_bytes], positions fp32 [num_rows, 3] (t, h, w; local
+ * to the new window), tags uint8 [num_rows] (H3_TAG_*), target uint8 [num_rows] (1 on groups 4
+ * and 5).  text [text_rows], clip_video [clip_video_frames * frame_h * frame_w], clip_audio
+ * [clip_audio_rows], new_video [new_video_frames * frame_h * frame_w], new_audio [new_audio_rows]
+ * rows; a source with no rows may be NULL.  row_bytes a positive multiple of 16; row pointers
+ * 16-byte aligned, pos 4-byte aligned.  rows must not overlap a source.
+ * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG, H3_ERR_MISALIGNED, H3_ERR_CUDA. */
+H3_API h3_status h3_continuation_pack(const h3_continuation_cfg* cfg, const void* text,
+                                      const void* clip_video, const void* clip_audio,
+                                      const void* new_video, const void* new_audio,
+                                      int32_t row_bytes, void* rows, float* pos, uint8_t* tag,
+                                      uint8_t* target, h3_stream_t stream);
+
+/* Overlap discard and append: new video frames [tail_frames, new_video_frames) are written after
+ * the clip's clip_video_frames frames, new audio rows [keep_audio_from, new_audio_rows) after its
+ * clip_audio_rows rows; the clip's existing rows are untouched.  clip_video / clip_audio are the
+ * clip's buffers with room for out_video_frames frames / out_audio_rows rows (capacities in rows
+ * are checked).  Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG, H3_ERR_MISALIGNED, H3_ERR_CUDA. */
+H3_API h3_status h3_continuation_append(const h3_continuation_cfg* cfg, const void* new_video,
+                                        const void* new_audio, int32_t row_bytes, void* clip_video,
+                                        int64_t clip_video_capacity_rows, void* clip_audio,
+                                        int64_t clip_audio_capacity_rows, h3_stream_t stream);
+
+/* Target-only update: dst row i = src row i where mask[i] != 0, other rows untouched.
+ * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG, H3_ERR_MISALIGNED, H3_ERR_CUDA. */
+H3_API h3_status h3_masked_row_update(void* dst, const void* src, const uint8_t* mask,
+                                      int32_t num_rows, int32_t row_bytes, h3_stream_t stream);
+
 /* Synchronises `stream`, returns the first device-side error recorded on the current device
  * since the last call (H3_OK if none) and clears it. */
 H3_API h3_status h3_get_device_error(h3_stream_t stream);

@@ -12,6 +12,8 @@ Calls:
   window_attn_fwd   shifted 3D window attention read and written in place on the grid
   vsa_select / vsa_attn_fwd   block-sparse video attention: block gate scores + top-k
                     selection, then attention over the selected 64-token blocks
+  continuation_plan / continuation_pack / continuation_append / masked_row_update
+                    continuation window: tails, five row groups, overlap discard, target updates
   get_device_error  read (and clear) the device-side error word
 """
 from __future__ import annotations
@@ -24,7 +26,9 @@ import torch
 
 __all__ = ["H3Error", "RopeConfig", "lib_path", "load_library", "rope_apply", "varlen_attn_fwd",
            "varlen_attn_fwd_noalloc", "window_attn_fwd", "vsa_block_count",
-           "vsa_select_workspace_size", "vsa_select", "vsa_attn_fwd",
+           "vsa_select_workspace_size", "vsa_select", "vsa_attn_fwd", "ContinuationConfig",
+           "ContinuationPlan", "continuation_config", "continuation_plan", "continuation_pack",
+           "continuation_append", "masked_row_update",
            "varlen_attn_workspace_size", "window_count", "window_pack", "window_unpack",
            "get_device_error", "TAG_TEXT", "TAG_VIDEO", "TAG_AUDIO"]
 
@@ -55,6 +59,23 @@ class RopeConfig(ctypes.Structure):
                 ("audio_hz", ctypes.c_float), ("video_fps", ctypes.c_float)]
 
 
+_I = ctypes.c_int32
+
+
+class ContinuationConfig(ctypes.Structure):
+    """Mirror of h3_continuation_cfg."""
+    _fields_ = [("text_rows", _I), ("clip_video_frames", _I), ("clip_audio_rows", _I),
+                ("frame_h", _I), ("frame_w", _I), ("new_video_frames", _I), ("new_audio_rows", _I),
+                ("tail_frames", _I), ("frames_per_latent", _I)]
+
+
+class ContinuationPlan(ctypes.Structure):
+    """Mirror of h3_continuation_plan."""
+    _fields_ = [("tail_start", _I), ("start_frame", _I), ("audio_cut", _I), ("group_rows", _I * 5),
+                ("group_offset", _I * 6), ("num_rows", _I), ("keep_video_from", _I),
+                ("keep_audio_from", _I), ("out_video_frames", _I), ("out_audio_rows", _I)]
+
+
 def lib_path() -> str:
     return os.path.join(_PKG_DIR, _LIB_NAME)
 
@@ -83,6 +104,11 @@ def load_library():
                                  I32, I32, P]),
         "h3_window_unpack": (I32, [P, I32, P, P, I32, P]),
         "h3_vsa_block_count": (I32, [I32P, I32P]),
+        "h3_continuation_make_plan": (I32, [ctypes.POINTER(ContinuationConfig), ctypes.POINTER(ContinuationPlan)]),
+        "h3_continuation_pack": (I32, [ctypes.POINTER(ContinuationConfig), P, P, P, P, P, I32, P, P, P, P, P]),
+        "h3_continuation_append": (I32, [ctypes.POINTER(ContinuationConfig), P, P, I32, P, ctypes.c_int64, P,
+                                         ctypes.c_int64, P]),
+        "h3_masked_row_update": (I32, [P, P, P, I32, I32, P]),
         "h3_vsa_select_workspace_size": (U64, [I32P, I32P, I32, I32]),
         "h3_vsa_select": (I32, [P, P, I32P, I32P, I32, I32, I32, F32, P, P, P, U64, P]),
         "h3_vsa_attn_fwd": (I32, [P, P, P, P, P, I32P, I32P, I32, I32, P, I32, F32, P]),
@@ -446,6 +472,88 @@ def vsa_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grid: Sequen
                                  _i3(block), H, D, _ptr(block_idx), topk, scale, _stream(dev))
     _check(st, "h3_vsa_attn_fwd")
     return (out, lse) if (return_lse or lse is not None) else out
+
+
+def continuation_config(text_rows: int, clip_video_frames: int, clip_audio_rows: int, frame_h: int,
+                        frame_w: int, new_video_frames: int, new_audio_rows: int, tail_frames: int = 7,
+                        frames_per_latent: int = 4) -> ContinuationConfig:
+    return ContinuationConfig(text_rows, clip_video_frames, clip_audio_rows, frame_h, frame_w,
+                              new_video_frames, new_audio_rows, tail_frames, frames_per_latent)
+
+
+def continuation_plan(cfg: ContinuationConfig) -> ContinuationPlan:
+    """Index math of a continuation window (host only)."""
+    plan = ContinuationPlan()
+    _check(load_library().h3_continuation_make_plan(ctypes.byref(cfg), ctypes.byref(plan)),
+           "h3_continuation_make_plan")
+    return plan
+
+
+def _rows2d(t: Optional[torch.Tensor], name: str):
+    if t is None:
+        return None, 0
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    return t, t[0].numel() * t.element_size() if t.shape[0] > 0 else 0
+
+
+def continuation_pack(cfg: ContinuationConfig, text, clip_video, clip_audio, new_video, new_audio,
+                      out: Optional[torch.Tensor] = None):
+    """The five-group DiT sequence of a continuation window: returns (rows, pos fp32 [N, 3],
+    tag u8 [N], target u8 [N]).  Row tensors are [n, ...] with one common row size."""
+    plan = continuation_plan(cfg)
+    srcs = [text, clip_video, clip_audio, new_video, new_audio]
+    ref = next(t for t in srcs if t is not None and t.shape[0] > 0)
+    dev = ref.device
+    row_bytes = ref[0].numel() * ref.element_size()
+    for i, t in enumerate(srcs):
+        if t is not None and t.shape[0] > 0:
+            _, rb = _rows2d(t, f"source {i}")
+            if rb != row_bytes or t.dtype != ref.dtype:
+                raise ValueError("all row tensors need the same row size and dtype")
+    n = plan.num_rows
+    out = torch.empty((n,) + tuple(ref.shape[1:]), dtype=ref.dtype, device=dev) if out is None else out
+    pos = torch.empty((n, 3), dtype=torch.float32, device=dev)
+    tag = torch.empty(n, dtype=torch.uint8, device=dev)
+    target = torch.empty(n, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = load_library().h3_continuation_pack(ctypes.byref(cfg), _ptr(text), _ptr(clip_video),
+                                                 _ptr(clip_audio), _ptr(new_video), _ptr(new_audio),
+                                                 row_bytes, _ptr(out), _ptr(pos), _ptr(tag), _ptr(target),
+                                                 _stream(dev))
+    _check(st, "h3_continuation_pack")
+    return out, pos, tag, target
+
+
+def continuation_append(cfg: ContinuationConfig, new_video: torch.Tensor, new_audio: torch.Tensor,
+                        clip_video: torch.Tensor, clip_audio: torch.Tensor):
+    """Append the new window's rows past the overlap to the clip buffers (in place; they must
+    have room for the plan's out_video_frames / out_audio_rows).  Returns the plan."""
+    plan = continuation_plan(cfg)
+    ref = new_video if new_video.shape[0] > 0 else new_audio
+    row_bytes = ref[0].numel() * ref.element_size()
+    dev = ref.device
+    hw = cfg.frame_h * cfg.frame_w
+    with torch.cuda.device(dev):
+        st = load_library().h3_continuation_append(ctypes.byref(cfg), _ptr(new_video), _ptr(new_audio),
+                                                   row_bytes, _ptr(clip_video), clip_video.shape[0],
+                                                   _ptr(clip_audio), clip_audio.shape[0], _stream(dev))
+    _check(st, "h3_continuation_append")
+    assert plan.out_video_frames * hw <= clip_video.shape[0]
+    return plan
+
+
+def masked_row_update(dst: torch.Tensor, src: torch.Tensor, mask: torch.Tensor) -> torch.Tensor:
+    """dst[i] = src[i] where mask[i] (uint8) is non-zero; in place on dst."""
+    if dst.shape != src.shape or dst.dtype != src.dtype or mask.dtype != torch.uint8:
+        raise ValueError("dst and src must match; mask must be uint8")
+    n = dst.shape[0]
+    row_bytes = dst[0].numel() * dst.element_size() if n > 0 else 16
+    with torch.cuda.device(dst.device):
+        st = load_library().h3_masked_row_update(_ptr(dst), _ptr(src), _ptr(mask), n, row_bytes,
+                                                 _stream(dst.device))
+    _check(st, "h3_masked_row_update")
+    return dst
 
 
 def get_device_error(device: Optional[torch.device] = None) -> int:

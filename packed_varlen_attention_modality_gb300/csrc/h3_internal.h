@@ -103,4 +103,20 @@ cudaError_t launch_vsa_select(const void* q, const void* k, const VsaGeom& g, in
                               int head_dim, int topk, float scale, float* scores, int32_t* sel,
                               void* workspace, cudaStream_t stream);
 
+// ---- continuation window ---------------------------------------------------------------------
+struct ContinuationGeom {
+  int offset[5];  // first packed row of each group (offset[0] = 0)
+  int num_rows;
+  int frame_h, frame_w;  // latent grid of a video frame
+};
+// src[k]: device base of group k's source rows; first_row[k]: its first source row.
+cudaError_t launch_continuation_pack(const ContinuationGeom& g, const void* const src[5],
+                                     const int64_t first_row[5], int row_bytes, void* rows,
+                                     float* pos, uint8_t* tag, uint8_t* target, cudaStream_t stream);
+// Two contiguous device copies (bytes multiples of 16, 16-byte aligned) in one launch.
+cudaError_t launch_copy_ranges(const void* const src[2], void* const dst[2], const int64_t bytes[2],
+                               cudaStream_t stream);
+cudaError_t launch_masked_row_update(void* dst, const void* src, const uint8_t* mask, int num_rows,
+                                     int row_bytes, cudaStream_t stream);
+
 }  // namespace h3

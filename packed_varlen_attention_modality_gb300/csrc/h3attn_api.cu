@@ -3,6 +3,7 @@
 // Nothing here allocates device memory.  The one piece of library-owned device state is the
 // error word below (a static __device__ variable, 4 bytes per device), where kernels record the
 // first device-side problem they meet (bad cu_seqlens, bad permutation entry, a timed-out wait).
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -366,6 +367,117 @@ h3_status h3_window_attn_fwd(const void* q, const void* k, const void* v, void* 
   a.err = device_error_ptr();
   if (a.err == nullptr) return H3_ERR_CUDA;
   return from_cuda(h3::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ---- continuation window ------------------------------------------------------------------------
+
+h3_status h3_continuation_make_plan(const h3_continuation_cfg* c, h3_continuation_plan* p) {
+  if (c == nullptr || p == nullptr) return H3_ERR_NULL;
+  if (c->text_rows < 0 || c->clip_video_frames < 0 || c->clip_audio_rows < 0 || c->frame_h <= 0 ||
+      c->frame_w <= 0 || c->new_video_frames < 0 || c->new_audio_rows < 0 || c->tail_frames < 0 ||
+      c->frames_per_latent <= 0)
+    return H3_ERR_INVALID_ARG;
+  const int64_t g0 = static_cast<int64_t>(c->clip_video_frames) - c->tail_frames;
+  if (g0 < 0 || c->new_video_frames < c->tail_frames) return H3_ERR_INVALID_ARG;
+  const int64_t s = g0 * c->frames_per_latent;
+  if (s > INT32_MAX / 40) return H3_ERR_INVALID_ARG;
+  const int64_t cut = std::min<int64_t>(s * 40 / 24, c->clip_audio_rows);  // floor(s * 40 / 24)
+  const int64_t ref_audio = c->clip_audio_rows - cut;
+  if (c->new_audio_rows < ref_audio) return H3_ERR_INVALID_ARG;
+  const int64_t hw = static_cast<int64_t>(c->frame_h) * c->frame_w;
+  const int64_t rows[5] = {c->text_rows, ref_audio, c->tail_frames * hw, c->new_audio_rows,
+                           c->new_video_frames * hw};
+  int64_t off = 0;
+  for (int k = 0; k < 5; ++k) {
+    p->group_offset[k] = static_cast<int32_t>(off);
+    off += rows[k];
+    if (off > INT32_MAX) return H3_ERR_INVALID_ARG;
+    p->group_rows[k] = static_cast<int32_t>(rows[k]);
+  }
+  p->group_offset[5] = static_cast<int32_t>(off);
+  p->num_rows = static_cast<int32_t>(off);
+  p->tail_start = static_cast<int32_t>(g0);
+  p->start_frame = static_cast<int32_t>(s);
+  p->audio_cut = static_cast<int32_t>(cut);
+  p->keep_video_from = c->tail_frames;
+  p->keep_audio_from = static_cast<int32_t>(ref_audio);
+  if (g0 + c->new_video_frames > INT32_MAX || cut + c->new_audio_rows > INT32_MAX)
+    return H3_ERR_INVALID_ARG;
+  p->out_video_frames = static_cast<int32_t>(g0 + c->new_video_frames);
+  p->out_audio_rows = static_cast<int32_t>(cut + c->new_audio_rows);
+  return H3_OK;
+}
+
+h3_status h3_continuation_pack(const h3_continuation_cfg* cfg, const void* text,
+                               const void* clip_video, const void* clip_audio,
+                               const void* new_video, const void* new_audio, int32_t row_bytes,
+                               void* rows, float* pos, uint8_t* tag, uint8_t* target,
+                               h3_stream_t stream) {
+  if (cfg == nullptr || rows == nullptr || pos == nullptr || tag == nullptr || target == nullptr)
+    return H3_ERR_NULL;
+  h3_continuation_plan p;
+  const h3_status st = h3_continuation_make_plan(cfg, &p);
+  if (st != H3_OK) return st;
+  if (row_bytes <= 0 || row_bytes % 16 != 0) return H3_ERR_INVALID_ARG;
+  const void* src[5] = {text, clip_audio, clip_video, new_audio, new_video};
+  for (int k = 0; k < 5; ++k) {
+    if (p.group_rows[k] > 0 && src[k] == nullptr) return H3_ERR_NULL;
+    if (src[k] != nullptr && !aligned16(src[k])) return H3_ERR_MISALIGNED;
+  }
+  if (static_cast<int64_t>(p.num_rows) * row_bytes / 16 > INT64_MAX / 4) return H3_ERR_INVALID_ARG;
+  if (!aligned16(rows) || (reinterpret_cast<uintptr_t>(pos) & 3u)) return H3_ERR_MISALIGNED;
+  const int64_t hw = static_cast<int64_t>(cfg->frame_h) * cfg->frame_w;
+  const int64_t first[5] = {0, p.audio_cut, static_cast<int64_t>(p.tail_start) * hw, 0, 0};
+  h3::ContinuationGeom g;
+  for (int k = 0; k < 5; ++k) g.offset[k] = p.group_offset[k];
+  g.num_rows = p.num_rows;
+  g.frame_h = cfg->frame_h;
+  g.frame_w = cfg->frame_w;
+  return from_cuda(h3::launch_continuation_pack(g, src, first, row_bytes, rows, pos, tag, target,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+h3_status h3_continuation_append(const h3_continuation_cfg* cfg, const void* new_video,
+                                 const void* new_audio, int32_t row_bytes, void* clip_video,
+                                 int64_t clip_video_capacity_rows, void* clip_audio,
+                                 int64_t clip_audio_capacity_rows, h3_stream_t stream) {
+  if (cfg == nullptr) return H3_ERR_NULL;
+  h3_continuation_plan p;
+  const h3_status st = h3_continuation_make_plan(cfg, &p);
+  if (st != H3_OK) return st;
+  if (row_bytes <= 0 || row_bytes % 16 != 0) return H3_ERR_INVALID_ARG;
+  const int64_t hw = static_cast<int64_t>(cfg->frame_h) * cfg->frame_w;
+  const int64_t v_rows = (static_cast<int64_t>(cfg->new_video_frames) - p.keep_video_from) * hw;
+  const int64_t a_rows = static_cast<int64_t>(cfg->new_audio_rows) - p.keep_audio_from;
+  if ((v_rows > 0 && (new_video == nullptr || clip_video == nullptr)) ||
+      (a_rows > 0 && (new_audio == nullptr || clip_audio == nullptr)))
+    return H3_ERR_NULL;
+  if (static_cast<int64_t>(p.out_video_frames) * hw > clip_video_capacity_rows && v_rows > 0)
+    return H3_ERR_INVALID_ARG;
+  if (p.out_audio_rows > clip_audio_capacity_rows && a_rows > 0) return H3_ERR_INVALID_ARG;
+  for (const void* ptr : {new_video, new_audio, static_cast<const void*>(clip_video),
+                          static_cast<const void*>(clip_audio)})
+    if (ptr != nullptr && !aligned16(ptr)) return H3_ERR_MISALIGNED;
+  const char* nv = static_cast<const char*>(new_video);
+  const char* na = static_cast<const char*>(new_audio);
+  char* cv = static_cast<char*>(clip_video);
+  char* ca = static_cast<char*>(clip_audio);
+  const void* src[2] = {v_rows > 0 ? nv + p.keep_video_from * hw * row_bytes : nullptr,
+                        a_rows > 0 ? na + static_cast<int64_t>(p.keep_audio_from) * row_bytes : nullptr};
+  void* dst[2] = {v_rows > 0 ? cv + cfg->clip_video_frames * hw * row_bytes : nullptr,
+                  a_rows > 0 ? ca + static_cast<int64_t>(cfg->clip_audio_rows) * row_bytes : nullptr};
+  const int64_t bytes[2] = {v_rows > 0 ? v_rows * row_bytes : 0, a_rows > 0 ? a_rows * row_bytes : 0};
+  return from_cuda(h3::launch_copy_ranges(src, dst, bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+h3_status h3_masked_row_update(void* dst, const void* src, const uint8_t* mask, int32_t num_rows,
+                               int32_t row_bytes, h3_stream_t stream) {
+  if (num_rows < 0 || row_bytes <= 0 || row_bytes % 16 != 0) return H3_ERR_INVALID_ARG;
+  if (num_rows == 0) return H3_OK;
+  if (dst == nullptr || src == nullptr || mask == nullptr) return H3_ERR_NULL;
+  if (!aligned16(dst) || !aligned16(src)) return H3_ERR_MISALIGNED;
+  return from_cuda(h3::launch_masked_row_update(dst, src, mask, num_rows, row_bytes,
+                                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // ---- VSA ----------------------------------------------------------------------------------------

@@ -194,3 +194,62 @@ def test_vsa_calls_reject_bad_arguments_on_the_host(lib):
     assert attn(topk=0) == 2 and attn(topk=9) == 2
     assert attn(D=64, block=_i3((2, 2, 2))) == 4
     assert attn(q=FAKE + 8) == 8 and attn(idx=FAKE + 2) == 8
+
+
+def _plan_fields(p):
+    return (p.tail_start, p.start_frame, p.audio_cut, tuple(p.group_rows), tuple(p.group_offset),
+            p.num_rows, p.keep_video_from, p.keep_audio_from, p.out_video_frames, p.out_audio_rows)
+
+
+def test_continuation_plan_matches_oracle_on_random_windows(lib):
+    import packed_varlen_attention_modality_gb300 as h3
+
+    rng = np.random.default_rng(21)
+    cases = [(558, 29, 200, 40, 50, 29, 200, 7, 4), (5, 245, 500, 2, 3, 20, 150, 7, 1),
+             (0, 7, 0, 1, 1, 7, 0, 7, 4), (3, 40, 9, 2, 2, 9, 30, 7, 4)]
+    for _ in range(200):
+        tail = int(rng.integers(0, 9))
+        clip_f = tail + int(rng.integers(0, 40))
+        fpl = int(rng.integers(1, 6))
+        clip_a = int(rng.integers(0, 400))
+        cut = min(((clip_f - tail) * fpl * 40) // 24, clip_a)
+        cases.append((int(rng.integers(0, 600)), clip_f, clip_a, int(rng.integers(1, 9)),
+                      int(rng.integers(1, 9)), tail + int(rng.integers(0, 40)),
+                      (clip_a - cut) + int(rng.integers(0, 300)), tail, fpl))
+    for c in cases:
+        ref = oracle.continuation_plan(*c[:7], tail_frames=c[7], frames_per_latent=c[8])
+        got = h3.continuation_plan(h3.continuation_config(*c))
+        assert _plan_fields(got) == (ref.tail_start, ref.start_frame, ref.audio_cut, ref.group_rows,
+                                     ref.group_offset, ref.num_rows, ref.keep_video_from,
+                                     ref.keep_audio_from, ref.out_video_frames, ref.out_audio_rows), c
+
+
+def test_continuation_calls_reject_bad_arguments_on_the_host(lib):
+    import packed_varlen_attention_modality_gb300 as h3
+
+    P = ctypes.c_void_p
+    bad = [h3.continuation_config(5, 6, 40, 2, 2, 10, 40),      # clip shorter than the tail
+           h3.continuation_config(5, 10, 40, 2, 2, 6, 40),      # new window shorter than the tail
+           h3.continuation_config(5, 29, 200, 2, 2, 29, 10),    # new audio shorter than the audio tail
+           h3.continuation_config(-1, 29, 200, 2, 2, 29, 200), h3.continuation_config(5, 29, 200, 0, 2, 29, 200)]
+    plan = h3.ContinuationPlan()
+    for c in bad:
+        assert lib.h3_continuation_make_plan(ctypes.byref(c), ctypes.byref(plan)) == 2
+    assert lib.h3_continuation_make_plan(None, ctypes.byref(plan)) == 1
+    good = h3.continuation_config(5, 29, 200, 2, 2, 29, 200)
+    f = lib.h3_continuation_pack
+
+    def pack(rb=64, rows=FAKE, text=FAKE):
+        return f(ctypes.byref(good), P(text) if text else None, P(FAKE), P(FAKE), P(FAKE), P(FAKE), rb,
+                 P(rows) if rows else None, P(FAKE), P(FAKE), P(FAKE), None)
+
+    assert pack(rows=0) == 1 and pack(text=0) == 1
+    assert pack(rb=24) == 2 and pack(rb=0) == 2
+    assert pack(rows=FAKE + 8) == 8
+    g = lib.h3_continuation_append
+    assert g(ctypes.byref(good), P(FAKE), P(FAKE), 64, P(FAKE), 10, P(FAKE), 10**6, None) == 2  # video capacity
+    assert g(ctypes.byref(good), P(FAKE), P(FAKE), 64, P(FAKE), 10**6, P(FAKE), 10, None) == 2  # audio capacity
+    assert g(ctypes.byref(good), None, P(FAKE), 64, P(FAKE), 10**6, P(FAKE), 10**6, None) == 1
+    m = lib.h3_masked_row_update
+    assert m(P(FAKE), P(FAKE), P(FAKE), 4, 24, None) == 2 and m(None, P(FAKE), P(FAKE), 4, 32, None) == 1
+    assert m(P(FAKE + 8), P(FAKE), P(FAKE), 4, 32, None) == 8 and m(None, None, None, 0, 32, None) == 0
