@@ -360,6 +360,50 @@ H3_API h3_status h3_continuation_append(const h3_continuation_cfg* cfg, const vo
 H3_API h3_status h3_masked_row_update(void* dst, const void* src, const uint8_t* mask,
                                       int32_t num_rows, int32_t row_bytes, h3_stream_t stream);
 
+/* ---- Window-aligned sequence parallelism: host-side plan ------------------------------------
+ * [H3-fast] "window attention across GPUs", "Window-aligned SP": whole windows (all heads) are the
+ * unit given to a GPU, so window attention stays local; regular and half-shifted layers
+ * alternate, and at each switch an all-to-all moves tokens to the owners of the new windows;
+ * cropped edge windows have unequal sizes, so windows are dealt out by token count, not by count.
+ * These calls do the integer planning only (host, no device work, no collective): the caller
+ * moves the rows with its own all-to-all.  Windows and shifts are as for h3_window_count. */
+
+/* Owner rank of every window of one layer: windows by size descending (ties: lower id) each go to
+ * the rank with the fewest tokens so far (ties: lower rank).
+ * window_rank: int32 [h3_window_count()] out; rank_tokens: int64 [world] out or NULL.
+ * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG. */
+H3_API h3_status h3_sp_assign_windows(const int32_t grid[3], const int32_t win[3],
+                                      const int32_t shift[3], int32_t world, int32_t* window_rank,
+                                      int64_t* rank_tokens);
+
+/* A rank's local row order in one layer: the original (row-major) index of each token it owns,
+ * its windows ascending and tokens row-major inside (the single-GPU packed order restricted to
+ * the rank).  order: int32 [rank_tokens[rank]] out (order_capacity entries available).
+ * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG (bad geometry, rank or owner, or capacity too small). */
+H3_API h3_status h3_sp_layer_order(const int32_t grid[3], const int32_t win[3],
+                                   const int32_t shift[3], const int32_t* window_rank,
+                                   int32_t world, int32_t rank, int32_t* order,
+                                   int64_t order_capacity);
+
+/* The all-to-all of a switch from layer `from` (shift_from, owners rank_from) to layer `to`,
+ * as seen by `rank`:
+ *   send_counts [world] out: rows this rank sends to each rank;
+ *   send_index  [sum send_counts] out: the rows of this rank's `from` layout to send, grouped by
+ *               destination rank ascending, each group in the destination's `to` order;
+ *   recv_counts [world] out: rows received from each rank;
+ *   recv_position [sum recv_counts] out: for the rows as they arrive (grouped by source rank
+ *               ascending, each group in this rank's `to` order), their row in this rank's `to`
+ *               layout.
+ * Gather by send_index, all-to-all with these counts, scatter to recv_position: the rank then
+ * holds its `to` windows in the order of h3_sp_layer_order.
+ * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG. */
+H3_API h3_status h3_sp_exchange_plan(const int32_t grid[3], const int32_t win[3],
+                                     const int32_t shift_from[3], const int32_t* rank_from,
+                                     const int32_t shift_to[3], const int32_t* rank_to,
+                                     int32_t world, int32_t rank, int64_t* send_counts,
+                                     int32_t* send_index, int64_t* recv_counts,
+                                     int32_t* recv_position);
+
 /* Synchronises `stream`, returns the first device-side error recorded on the current device
  * since the last call (H3_OK if none) and clears it. */
 H3_API h3_status h3_get_device_error(h3_stream_t stream);

@@ -14,6 +14,10 @@ Calls:
                     selection, then attention over the selected 64-token blocks
   continuation_plan / continuation_pack / continuation_append / masked_row_update
                     continuation window: tails, five row groups, overlap discard, target updates
+  sp_assign_windows / sp_layer_order / sp_exchange_plan / sp_exchange
+                    window-aligned sequence parallelism: window owners, local orders, the
+                    all-to-all of a regular <-> shifted switch (planning native, rows moved by
+                    torch.distributed)
   get_device_error  read (and clear) the device-side error word
 """
 from __future__ import annotations
@@ -28,7 +32,8 @@ __all__ = ["H3Error", "RopeConfig", "lib_path", "load_library", "rope_apply", "v
            "varlen_attn_fwd_noalloc", "window_attn_fwd", "vsa_block_count",
            "vsa_select_workspace_size", "vsa_select", "vsa_attn_fwd", "ContinuationConfig",
            "ContinuationPlan", "continuation_config", "continuation_plan", "continuation_pack",
-           "continuation_append", "masked_row_update",
+           "continuation_append", "masked_row_update", "sp_assign_windows", "sp_layer_order",
+           "sp_rank_tokens", "sp_exchange_plan", "sp_exchange",
            "varlen_attn_workspace_size", "window_count", "window_pack", "window_unpack",
            "get_device_error", "TAG_TEXT", "TAG_VIDEO", "TAG_AUDIO"]
 
@@ -109,6 +114,9 @@ def load_library():
         "h3_continuation_append": (I32, [ctypes.POINTER(ContinuationConfig), P, P, I32, P, ctypes.c_int64, P,
                                          ctypes.c_int64, P]),
         "h3_masked_row_update": (I32, [P, P, P, I32, I32, P]),
+        "h3_sp_assign_windows": (I32, [I32P, I32P, I32P, I32, P, P]),
+        "h3_sp_layer_order": (I32, [I32P, I32P, I32P, P, I32, I32, P, ctypes.c_int64]),
+        "h3_sp_exchange_plan": (I32, [I32P, I32P, I32P, P, I32P, P, I32, I32, P, P, P, P]),
         "h3_vsa_select_workspace_size": (U64, [I32P, I32P, I32, I32]),
         "h3_vsa_select": (I32, [P, P, I32P, I32P, I32, I32, I32, F32, P, P, P, U64, P]),
         "h3_vsa_attn_fwd": (I32, [P, P, P, P, P, I32P, I32P, I32, I32, P, I32, F32, P]),
@@ -554,6 +562,84 @@ def masked_row_update(dst: torch.Tensor, src: torch.Tensor, mask: torch.Tensor) 
                                                  _stream(dst.device))
     _check(st, "h3_masked_row_update")
     return dst
+
+
+def _np_ptr(a):
+    return ctypes.c_void_p(a.ctypes.data) if a is not None and a.size else None
+
+
+def sp_assign_windows(grid: Sequence[int], win: Sequence[int], shift: Sequence[int], world: int):
+    """Owner rank of every window of one layer (longest-first on token counts) and the tokens
+    each rank owns: (window_rank int32 [nwin], rank_tokens int64 [world]) as numpy arrays."""
+    import numpy as np
+
+    owner = np.empty(window_count(grid, win, shift), dtype=np.int32)
+    tokens = np.empty(int(world), dtype=np.int64)
+    _check(load_library().h3_sp_assign_windows(_i3(grid), _i3(win), _i3(shift), int(world),
+                                               _np_ptr(owner), _np_ptr(tokens)), "h3_sp_assign_windows")
+    return owner, tokens
+
+
+def sp_layer_order(grid, win, shift, window_rank, world: int, rank: int):
+    """Original token indices a rank holds in one layer, in its local order (numpy int32)."""
+    import numpy as np
+
+    owner = np.ascontiguousarray(window_rank, dtype=np.int32)
+    n = int(sp_rank_tokens(grid, win, shift, owner, world)[rank])
+    order = np.empty(max(n, 1), dtype=np.int32)
+    _check(load_library().h3_sp_layer_order(_i3(grid), _i3(win), _i3(shift), _np_ptr(owner), int(world),
+                                            int(rank), _np_ptr(order), n), "h3_sp_layer_order")
+    return order[:n]
+
+
+def sp_rank_tokens(grid, win, shift, window_rank, world: int):
+    """Tokens each rank owns under a given window -> rank map (numpy int64 [world])."""
+    import numpy as np
+
+    owner = np.asarray(window_rank, dtype=np.int64)
+    sizes = np.empty(owner.size, np.int64)
+    nw = [(int(L) + int(s) + int(w) - 1) // int(w) for L, w, s in zip(grid, win, shift)]
+    axes = [np.array([min(L, (i + 1) * w - s) - max(0, i * w - s) for i in range(n)])
+            for L, w, s, n in zip(grid, win, shift, nw)]
+    sizes[:] = np.einsum("i,j,k->ijk", *axes).reshape(-1)
+    return np.bincount(owner, weights=sizes, minlength=int(world)).astype(np.int64)
+
+
+def sp_exchange_plan(grid, win, shift_from, rank_from, shift_to, rank_to, world: int, rank: int):
+    """All-to-all of a layer switch seen by one rank: dict of numpy arrays send_counts,
+    send_index, recv_counts, recv_position (see h3_sp_exchange_plan)."""
+    import numpy as np
+
+    a = np.ascontiguousarray(rank_from, dtype=np.int32)
+    b = np.ascontiguousarray(rank_to, dtype=np.int32)
+    n_from = int(sp_rank_tokens(grid, win, shift_from, a, world)[rank])
+    n_to = int(sp_rank_tokens(grid, win, shift_to, b, world)[rank])
+    plan = dict(send_counts=np.empty(int(world), np.int64), send_index=np.empty(max(n_from, 1), np.int32),
+                recv_counts=np.empty(int(world), np.int64), recv_position=np.empty(max(n_to, 1), np.int32))
+    _check(load_library().h3_sp_exchange_plan(_i3(grid), _i3(win), _i3(shift_from), _np_ptr(a), _i3(shift_to),
+                                              _np_ptr(b), int(world), int(rank),
+                                              _np_ptr(plan["send_counts"]), _np_ptr(plan["send_index"]),
+                                              _np_ptr(plan["recv_counts"]), _np_ptr(plan["recv_position"])),
+           "h3_sp_exchange_plan")
+    plan["send_index"] = plan["send_index"][:n_from]
+    plan["recv_position"] = plan["recv_position"][:n_to]
+    return plan
+
+
+def sp_exchange(x_local: torch.Tensor, plan, group=None) -> torch.Tensor:
+    """Move a rank's rows from its `from` layout to its `to` layout: gather by the plan's send
+    index, one all_to_all_single, scatter to the receive positions (torch.distributed)."""
+    import torch.distributed as dist
+
+    dev = x_local.device
+    send = x_local.index_select(0, torch.from_numpy(plan["send_index"]).long().to(dev))
+    n_to = int(plan["recv_counts"].sum())
+    recv = torch.empty((n_to,) + tuple(x_local.shape[1:]), dtype=x_local.dtype, device=dev)
+    dist.all_to_all_single(recv, send, output_split_sizes=[int(c) for c in plan["recv_counts"]],
+                           input_split_sizes=[int(c) for c in plan["send_counts"]], group=group)
+    out = torch.empty_like(recv)
+    out[torch.from_numpy(plan["recv_position"]).long().to(dev)] = recv
+    return out
 
 
 def get_device_error(device: Optional[torch.device] = None) -> int:

@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libh3attn.so")
 
 SOURCES = ["h3attn_api.cu", "rope_kernel.cu", "window_kernel.cu", "attn_fwd_sm103.cu",
-           "vsa_kernel.cu", "continuation_kernel.cu"]
+           "vsa_kernel.cu", "continuation_kernel.cu", "sp_planner.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]
