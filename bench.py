@@ -44,7 +44,7 @@ def parse_args():
     p.add_argument("--workload", default="h3_full_request",
                    choices=["h3_full_request", "single_request_4k", "continuation_batch",
                             "video_segment_16k", "window_grid", "window_grid_16x24x84",
-                            "vsa_video", "vsa_video_16x24x84", "continuation_window"],
+                            "vsa_video", "vsa_video_16x24x84", "continuation_window", "tiny_example"],
                    help="h3_full_request is the metric's workload; the others are side measurements")
     return p.parse_args()
 
@@ -231,6 +231,8 @@ def run_ours(args, rank, world, local_rank):
         return run_vsa(args, rank, world, dev, h3, peaks)
     if args.workload == "continuation_window":
         return run_continuation(args, rank, world, dev, h3, peaks)
+    if args.workload == "tiny_example":
+        return run_latency(args, rank, world, dev, h3)
     headline = args.workload == "h3_full_request"
     wl = workloads.WORKLOADS[args.workload]()
     H, D, C, N = wl.num_heads, wl.head_dim, wl.capacity, wl.num_tokens
@@ -696,6 +698,64 @@ def run_continuation(args, rank, world, dev, h3, peaks):
                          "kernel": "continuation_pack_kernel",
                          "peak_source": "%s (copy bandwidth)" % peaks["source"]},
             "clocks": clocks, "gpu_launches": 3 * args.steps}), flush=True)
+
+
+def run_latency(args, rank, world, dev, h3):
+    """The pages' worked example (45 tokens, segments [0,10,30,45], 2 x 64): launch-latency bound,
+    so it is reported in microseconds per step (RoPE + attention plan + attention), issued
+    eagerly and as one replayed CUDA graph."""
+    import workloads
+
+    wl = workloads.tiny_example(capacity=64)
+    H, D, N = wl.num_heads, wl.head_dim, wl.num_tokens
+    q, k, v = (t.to(dev) for t in (wl.q, wl.k, wl.v))
+    pos, tag = torch.from_numpy(wl.pos).to(dev), torch.from_numpy(wl.tag).to(dev)
+    cu, cu_req = torch.from_numpy(wl.cu_seqlens).to(dev), torch.from_numpy(wl.cu_requests).to(dev)
+    frames = torch.from_numpy(wl.start_frames).to(dev)
+    qr, kr, o = torch.empty_like(q), torch.empty_like(k), torch.empty_like(q)
+    ws = torch.empty(max(16, h3.varlen_attn_workspace_size(wl.num_segments, H, wl.max_seqlen, D)),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        h3.rope_apply(q, k, pos, tag, cu_req, frames, num_tokens=N, q_out=qr, k_out=kr)
+        h3.varlen_attn_fwd(qr, kr, v, cu, wl.max_seqlen, out=o, workspace=ws)
+
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        for _ in range(max(3, args.warmup)):
+            step()
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step()
+    torch.cuda.synchronize(dev)
+    if h3.get_device_error(dev) != 0:
+        raise RuntimeError("device error during warm-up")
+    reps = max(100, 100 * args.steps)
+
+    def timed(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(reps):
+                fn()
+            e1.record(s)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    eager_us, graph_us = timed(step), timed(graph.replay)
+    if h3.get_device_error(dev) != 0:
+        raise RuntimeError("device error during the timed steps")
+    if rank == 0:
+        print(json.dumps({
+            "metric": "worked-example step latency (RoPE + varlen attention, 45 tokens)",
+            "value": graph_us, "unit": "us", "n_gpus": world, "steps": reps, "warmup": max(3, args.warmup),
+            "ms_per_step": graph_us / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "tokens": N, "cu_seqlens": [int(x) for x in wl.cu_seqlens],
+                       "heads": H, "head_dim": D},
+            "latency_us": {"cuda_graph_replay": graph_us, "eager": eager_us},
+            "gpu_launches": 3 * reps}), flush=True)
 
 
 def _block_sizes(grid, block):

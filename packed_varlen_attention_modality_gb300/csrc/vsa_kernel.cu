@@ -10,14 +10,15 @@
 //
 // Three kernels, all HBM- or FFMA-bound (the gate is ~1 % of the fine attention's work):
 //   vsa_pool_kernel    mean of each block's Q and K rows per head (fp32 sums in token order)
-//   vsa_score_kernel   S_h = scale * Qmean_h Kmean_h^T, a 32 x 128 output tile per CTA with
-//                      4 x 4 register micro-tiles (one broadcast and one float4 shared load per
-//                      16 FFMA), written to the caller's [H, nblk, nblk] score buffer
+//   vsa_score_kernel   S_h = scale * Qmean_h Kmean_h^T, a 64 x 256 output tile per CTA with
+//                      8 x 8 register micro-tiles (two broadcast and two float4 shared loads per
+//                      64 FFMA), written to the caller's [H, nblk, nblk] score buffer
 //   vsa_topk_kernel    one warp per (head, query block): 8-bit radix select of the k-th largest
 //                      score over 4 passes (the row stays in L2), then an ascending ballot
 //                      compaction that takes the ties at the threshold lowest id first
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "h3_internal.h"
@@ -26,10 +27,11 @@ namespace h3 {
 namespace {
 
 constexpr int kPoolThreads = 256;
-constexpr int kScoreRows = 32;     // query blocks per score tile
-constexpr int kScoreCols = 128;    // key blocks per score tile
+constexpr int kScoreRows = 64;     // query blocks per score tile
+constexpr int kScoreCols = 256;    // key blocks per score tile
 constexpr int kScoreThreads = 256;
 constexpr int kTopkWarps = 8;
+constexpr size_t kTopkStageBytes = 200 * 1024;  // shared memory for staged score rows
 
 // Block b of the grid: origin and extent (cropped by the grid edge).
 struct BlockBox {
@@ -83,8 +85,10 @@ vsa_pool_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   }
 }
 
-// grid (ceil(nblk / 128), ceil(nblk / 32), heads).  Thread (rg, kg) = (tid / 32, tid % 32)
-// computes query blocks 4 rg .. 4 rg + 3 against key blocks 4 kg .. 4 kg + 3 of the tile.
+// grid (ceil(nblk / 256), ceil(nblk / 64), heads).  Thread (rg, kg) = (tid / 32, tid % 32)
+// computes query blocks 8 rg .. 8 rg + 7 against key blocks 4 kg .. 4 kg + 3 and
+// 128 + 4 kg .. 128 + 4 kg + 3 of the tile: per dimension two broadcast and two conflict-free
+// float4 shared loads feed 64 FFMA, so the FMA pipes, not shared memory, set the pace.
 constexpr int kQs = kScoreRows + 4;  // padded smem row lengths (float4 alignment kept)
 constexpr int kKs = kScoreCols + 4;
 template <int D>
@@ -113,25 +117,28 @@ vsa_score_kernel(const float* __restrict__ qm, const float* __restrict__ km, int
   }
   __syncthreads();
   const int rg = threadIdx.x >> 5, kg = threadIdx.x & 31;
-  float acc[4][4] = {};
-#pragma unroll 8
+  float acc[8][8] = {};
+#pragma unroll 4
   for (int d = 0; d < D; ++d) {
-    const float4 a = *reinterpret_cast<const float4*>(&qs[d * kQs + 4 * rg]);
-    const float4 b = *reinterpret_cast<const float4*>(&ks[d * kKs + 4 * kg]);
-    const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+    const float4 a0 = *reinterpret_cast<const float4*>(&qs[d * kQs + 8 * rg]);
+    const float4 a1 = *reinterpret_cast<const float4*>(&qs[d * kQs + 8 * rg + 4]);
+    const float4 b0 = *reinterpret_cast<const float4*>(&ks[d * kKs + 4 * kg]);
+    const float4 b1 = *reinterpret_cast<const float4*>(&ks[d * kKs + 128 + 4 * kg]);
+    const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+      for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = r0 + 4 * rg + i;
+  for (int i = 0; i < 8; ++i) {
+    const int r = r0 + 8 * rg + i;
     if (r >= nblk) break;
     float* row = scores + (static_cast<size_t>(h) * nblk + r) * nblk;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = c0 + 4 * kg + j;
+    for (int j = 0; j < 8; ++j) {
+      const int c = c0 + (j < 4 ? 4 * kg + j : 128 + 4 * kg + (j - 4));
       if (c < nblk) row[c] = acc[i][j] * scale;
     }
   }
@@ -143,16 +150,25 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// One warp per (head, query block) row of the score matrix.
+// One warp per (head, query block) row of the score matrix.  With `stage` set, each warp first
+// copies its row into shared memory (blockDim.x / 32 rows of nblk floats, dynamic) and runs the
+// five passes there; otherwise they re-read the row from global memory.
 __global__ void __launch_bounds__(kTopkWarps * 32)
 vsa_topk_kernel(const float* __restrict__ scores, int rows, int nblk, int topk,
-                int32_t* __restrict__ sel) {
+                int32_t* __restrict__ sel, int stage) {
+  extern __shared__ float topk_rows[];
   __shared__ uint32_t hist_all[kTopkWarps][256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kTopkWarps + warp;
+  const int row = blockIdx.x * (blockDim.x >> 5) + warp;
   if (row >= rows) return;
   uint32_t* hist = hist_all[warp];
   const float* s = scores + static_cast<size_t>(row) * nblk;
+  if (stage) {
+    float* mine = topk_rows + static_cast<size_t>(warp) * nblk;
+    for (int i = lane; i < nblk; i += 32) mine[i] = s[i];
+    __syncwarp();
+    s = mine;
+  }
   // radix select of the topk-th largest key, 8 bits per pass from the top
   uint32_t prefix = 0, mask = 0;
   int remaining = topk;  // how many of the wanted keys still lie at or below the current prefix
@@ -219,6 +235,21 @@ vsa_topk_kernel(const float* __restrict__ scores, int rows, int nblk, int topk,
   }
 }
 
+cudaError_t configure_topk() {
+  static bool configured[64] = {};  // the shared-memory opt-in is made once per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(vsa_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kTopkStageBytes));
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  return cudaSuccess;
+}
+
 template <int D>
 cudaError_t launch_score(dim3 grid, const float* qm, const float* km, int nblk, float scale,
                          float* scores, cudaStream_t stream) {
@@ -262,8 +293,16 @@ cudaError_t launch_vsa_select(const void* q, const void* k, const VsaGeom& g, in
                       : launch_score<64>(sgrid, qm, km, nblk, scale, scores, stream);
   if (e != cudaSuccess) return e;
   const int rows = heads * nblk;
-  vsa_topk_kernel<<<(rows + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, stream>>>(
-      scores, rows, nblk, topk, sel);
+  // rows staged in shared memory when at least one fits in the opt-in budget
+  const size_t row_bytes = static_cast<size_t>(nblk) * sizeof(float);
+  const int warps = static_cast<int>(std::min<size_t>(kTopkWarps, kTopkStageBytes / row_bytes));
+  const int stage = warps >= 1 ? 1 : 0;
+  const int per_cta = stage ? warps : kTopkWarps;
+  e = configure_topk();
+  if (e != cudaSuccess) return e;
+  vsa_topk_kernel<<<(rows + per_cta - 1) / per_cta, per_cta * 32,
+                    stage ? static_cast<size_t>(per_cta) * row_bytes : 0, stream>>>(
+      scores, rows, nblk, topk, sel, stage);
   return cudaGetLastError();
 }
 
