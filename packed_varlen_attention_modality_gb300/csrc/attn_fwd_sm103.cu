@@ -1,4 +1,11 @@
-// Packed varlen (block-diagonal) softmax attention forward for sm_103a: TMA + tcgen05 + TMEM.
+// Softmax attention forward for sm_103a: TMA + tcgen05 + TMEM, in three variants of one kernel
+// template (the warp roles, rings, barriers and TMEM plan below are shared):
+//   kModePacked  block-diagonal attention over the cu_seqlens segments of a packed sequence;
+//   kModeWindow  3D (shifted) window attention read and written in place on a (T, H, W) grid:
+//                a 128-row tile is one 5-D TMA box of whole window frames, edge windows masked;
+//   kModeVsa     block-sparse video attention: a tile holds two 64-token query blocks, each
+//                attending to its own selected key blocks, stacked in every key/value tile.
+// The description below is that of the packed variant; the others differ where noted in code.
 //
 // [H3-vLLM] "Joint audio/video generation in production: MiniMax-H3 and vLLM-Omni", sec. 3:
 // cu_seqlens holds the offsets of the sub-sequences packed into one sequence; a query of
