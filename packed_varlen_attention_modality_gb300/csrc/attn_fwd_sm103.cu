@@ -96,6 +96,8 @@ struct WorkDesc {
   int box[3];     // window: grid (t, h, w) of the first valid tile's box origin (may be < 0)
   int ntiles;     // window / VSA: query tiles of the item (1 or 2)
   int nkv;        // window / VSA: key/value steps of the item
+  int hbox;       // window: box rows along H (the window's, or half of it for an edge window)
+  int fpt;        // window: frames per 128-row tile (128 / (hbox * window W))
   uint32_t mask[2][4];  // window: rows of each tile that lie inside the grid (= inside the window)
 };
 
@@ -133,6 +135,9 @@ __device__ __forceinline__ uint64_t low_bits(int n) {  // n in [0, 64]
 // one time read neighbouring 256-byte pieces of the same token rows.  Along each axis the window's
 // box starts at i * w - s (the shifted grid; may be negative) and the rows inside the grid are
 // [max(0, start), min(L, start + w)): the rest of the box is zero-filled by TMA and masked.
+// An edge window whose rows inside the grid along H fit in half the window (g.half_h) uses the
+// half-height box, starting at its first valid row, with twice the frames per tile: the shifted
+// layer's top and bottom windows then take one tile instead of two.
 // The masks are built in registers: a frame mask (valid h rows x valid w run), then per tile the
 // valid frames of that tile.
 __device__ __forceinline__ WorkDesc decode_window(uint32_t item, const WindowAttnGeom& g,
@@ -146,19 +151,23 @@ __device__ __forceinline__ WorkDesc decode_window(uint32_t item, const WindowAtt
   const int vl_t = max(0, -lo_t), vh_t = min(g.w[0], g.L[0] - lo_t);
   const int vl_h = max(0, -lo_h), vh_h = min(g.w[1], g.L[1] - lo_h);
   const int vl_w = max(0, -lo_w), vh_w = min(g.w[2], g.L[2] - lo_w);
-  const int bt = g.frames_per_tile;
+  const bool half = g.half_h && 2 * (vh_h - vl_h) <= g.w[1];
+  const int h0 = half ? vl_h : 0;  // first box row along H, relative to the window
+  d.hbox = half ? g.w[1] / 2 : g.w[1];
+  d.fpt = half ? 2 * g.frames_per_tile : g.frames_per_tile;
+  const int bt = d.fpt;
   const int tile_lo = vl_t / bt, tile_hi = (vh_t + bt - 1) / bt;
   d.ntiles = tile_hi - tile_lo;
   d.nkv = d.ntiles;
   d.box[0] = lo_t + tile_lo * bt;
-  d.box[1] = lo_h;
+  d.box[1] = lo_h + h0;
   d.box[2] = lo_w;
-  // frame mask: bits fh * ww + fw for valid (fh, fw); ww <= 128 and pf = wh * ww <= 128
-  const int ww = g.w[2], pf = g.w[1] * g.w[2];
+  // frame mask: bits fh * ww + fw for valid (fh, fw) of the box; ww <= 128, pf = hbox * ww <= 128
+  const int ww = g.w[2], pf = d.hbox * g.w[2];
   uint64_t flo = 0, fhi = 0;
   const int run = vh_w - vl_w;
   const uint64_t rlo = low_bits(min(run, 64)), rhi = run > 64 ? low_bits(run - 64) : 0ull;
-  for (int fh = vl_h; fh < vh_h; ++fh) or_shifted(flo, fhi, rlo, rhi, fh * ww + vl_w);
+  for (int fh = vl_h - h0; fh < vh_h - h0; ++fh) or_shifted(flo, fhi, rlo, rhi, fh * ww + vl_w);
 #pragma unroll
   for (int k = 0; k < 2; ++k) {  // ntiles <= 2: frames_per_tile * 2 covers the window's frames
     if (k >= d.ntiles) break;
@@ -324,12 +333,12 @@ struct Cfg {
   static constexpr int kBoxes = D / 64;               // 64-column (128-byte) swizzle boxes
   static constexpr int kTileBytes = kBlockM * D * 2;  // one Q, K or V tile
   static constexpr int kBoxBytes = kBlockM * 128;     // one 128-row box
-  // Ring depths (5 tiles of 32 KB fit beside the two Q tiles at D = 128).  Shared key/value
-  // tiles: 3 K + 2 V.  VSA, where every step takes a K and a V tile per query tile: 2 K + 3 V
-  // (a V tile is loaded only once the PV product two entries back has drained, so V needs the
-  // deeper ring; measured 50 -> 39 ms on the 1344x768 latent).
-  static constexpr int kStagesK = (D == 128) ? (kMode == kModeVsa ? 2 : 3) : 4;
-  static constexpr int kStagesV = (D == 128) ? (kMode == kModeVsa ? 3 : 2) : 4;
+  // Ring depths (5 tiles of 32 KB fit beside the two Q tiles at D = 128).  Packed segments:
+  // 3 K + 2 V.  The grid variants: 2 K + 3 V -- a V tile is loaded only once the PV product two
+  // entries back has drained, so V gains most from depth (VSA, which takes a K and a V tile per
+  // query tile per step: 50 -> 39 ms on the 1344x768 latent; windows: 1-1.5 %).
+  static constexpr int kStagesK = (D == 128) ? (kMode == kModePacked ? 3 : 2) : 4;
+  static constexpr int kStagesV = (D == 128) ? (kMode == kModePacked ? 2 : 3) : 4;
   // q_full[2], q_empty, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
   // p_full[2], o_final[2], o_empty[2], w_full[2], w_empty[2], drain
   static constexpr int kNumBars = 3 + 2 * kStagesK + 2 * kStagesV + 12 + 1;
@@ -378,7 +387,10 @@ template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 const __grid_constant__ CUtensorMap tmap_k,
-                const __grid_constant__ CUtensorMap tmap_v, __nv_bfloat16* __restrict__ out,
+                const __grid_constant__ CUtensorMap tmap_v,
+                const __grid_constant__ CUtensorMap tmap_q2,  // windows: half-height boxes
+                const __grid_constant__ CUtensorMap tmap_k2,
+                const __grid_constant__ CUtensorMap tmap_v2, __nv_bfloat16* __restrict__ out,
                 float* __restrict__ lse, const int32_t* __restrict__ cu_seqlens, int num_segments,
                 int capacity, int num_heads, float scale, float scale_log2,
                 uint32_t* __restrict__ ws, const __grid_constant__ WindowAttnGeom wg,
@@ -425,6 +437,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     tma_prefetch_desc(&tmap_q);
     tma_prefetch_desc(&tmap_k);
     tma_prefetch_desc(&tmap_v);
+    if (kWin && wg.half_h) {
+      tma_prefetch_desc(&tmap_q2);
+      tma_prefetch_desc(&tmap_k2);
+      tma_prefetch_desc(&tmap_v2);
+    }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_qfull(t), 1);
       mbar_init(bar_sfull(t), 1);
@@ -535,13 +552,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           const ItemShape sh = shape_of<kMode>(d);
           const bool has1 = sh.has1;
           const int nkv = sh.nkv;
-          // tile loads: packed rows [row, row + 128) of one head; window box (w, h, t) of frames
+          // tile loads: packed rows [row, row + 128) of one head; window box (w, h, t) of frames,
+          // from the half-height map for a half edge window
+          const bool hhalf = kWin && d.hbox != wg.w[1];
           auto load_tile = [&](uint8_t* dst, const CUtensorMap* map, int tile, int row,
                                uint32_t bar) {
             for (int b = 0; b < C::kBoxes; ++b) {
               if constexpr (kWin)
                 tma_load_5d(smem_u32(dst + b * C::kBoxBytes), map, b * 64, d.head, d.box[2],
-                            d.box[1], d.box[0] + tile * wg.frames_per_tile, bar);
+                            d.box[1], d.box[0] + tile * d.fpt, bar);
               else
                 tma_load_3d(smem_u32(dst + b * C::kBoxBytes), map, b * 64, d.head, row, bar);
             }
@@ -565,7 +584,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           } else {
             for (int t = 0; t < (has1 ? 2 : 1); ++t) {
               mbar_arrive_expect_tx(bar_qfull(t), C::kTileBytes);
-              load_tile(sQ + t * C::kTileBytes, &tmap_q, t, d.q0 + t * kBlockM, bar_qfull(t));
+              load_tile(sQ + t * C::kTileBytes, hhalf ? &tmap_q2 : &tmap_q, t, d.q0 + t * kBlockM, bar_qfull(t));
               ++qn[t];
             }
             for (int j = 0; j < nkv && ok; ++j) {
@@ -574,13 +593,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
               ok = mbar_wait(bar_kempty(s), ((kt / SK) & 1) ^ 1);
               if (!ok) break;
               mbar_arrive_expect_tx(bar_kfull(s), C::kTileBytes);
-              load_tile(sK + s * C::kTileBytes, &tmap_k, j, row, bar_kfull(s));
+              load_tile(sK + s * C::kTileBytes, hhalf ? &tmap_k2 : &tmap_k, j, row, bar_kfull(s));
               ++kt;
               const int v = static_cast<int>(vt % SV);
               ok = mbar_wait(bar_vempty(v), ((vt / SV) & 1) ^ 1);
               if (!ok) break;
               mbar_arrive_expect_tx(bar_vfull(v), C::kTileBytes);
-              load_tile(sV + v * C::kTileBytes, &tmap_v, j, row, bar_vfull(v));
+              load_tile(sV + v * C::kTileBytes, hhalf ? &tmap_v2 : &tmap_v, j, row, bar_vfull(v));
               ++vt;
             }
           }
@@ -997,9 +1016,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 gw < wg.L[2];
         q_row = (gt * wg.L[1] + gh) * wg.L[2] + gw;
       } else if constexpr (kWin) {
-        const int pf = wg.w[1] * wg.w[2];
-        const int gt = d.box[0] + t * wg.frames_per_tile + row / pf;
-        const int gh = d.box[1] + (row / wg.w[2]) % wg.w[1];
+        const int pf = d.hbox * wg.w[2];
+        const int gt = d.box[0] + t * d.fpt + row / pf;
+        const int gh = d.box[1] + (row / wg.w[2]) % d.hbox;
         const int gw = d.box[2] + row % wg.w[2];
         uint32_t word = 0;
 #pragma unroll
@@ -1101,8 +1120,10 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
   if (max_items <= 0) return cudaSuccess;
   const int grid = static_cast<int>(max_items < want ? max_items : want);
   const float scale_log2 = a.scale * 1.4426950408889634f;
+  const bool half = kMode == kModeWindow && a.wg.half_h;  // the half-height maps were built
   attn_fwd_kernel<D, kMode><<<grid, kThreads, C::kSmemBytes, stream>>>(
-      a.tmap_q, a.tmap_k, a.tmap_v, static_cast<__nv_bfloat16*>(a.o), a.lse, a.cu_seqlens,
+      a.tmap_q, a.tmap_k, a.tmap_v, half ? a.tmap_q2 : a.tmap_q, half ? a.tmap_k2 : a.tmap_k,
+      half ? a.tmap_v2 : a.tmap_v, static_cast<__nv_bfloat16*>(a.o), a.lse, a.cu_seqlens,
       a.num_segments, a.capacity, a.num_heads, a.scale, scale_log2, ws, a.wg, a.vsa_sel, a.err);
   return cudaGetLastError();
 }

@@ -65,12 +65,15 @@ struct WindowAttnGeom {
   int s[3];
   int nwin[3];
   int frames_per_tile;
+  int half_h;  // windows: half-height maps exist (window H even) for edge windows
   int topk;
 };
 
 struct AttnArgs {
   // packed: 3-D views {D, H, capacity} of Q, K, V; window: 5-D views {D, H, W, Hgrid, T}
   CUtensorMap tmap_q, tmap_k, tmap_v;
+  // window: the same views with half-height boxes (edge windows); otherwise copies of the above
+  CUtensorMap tmap_q2, tmap_k2, tmap_v2;
   int mode;            // kAttnModePacked / kAttnModeWindow / kAttnModeVsa
   WindowAttnGeom wg;
   const int32_t* vsa_sel;  // VSA: [num_heads, nblk, topk] selected key blocks

@@ -358,6 +358,15 @@ h3_status h3_window_attn_fwd(const void* q, const void* k, const void* v, void* 
       !make_window_map(&a.tmap_k, k, grid, win, frames, num_heads, head_dim) ||
       !make_window_map(&a.tmap_v, v, grid, win, frames, num_heads, head_dim))
     return H3_ERR_CUDA;
+  // half-height boxes for edge windows with at most half their rows along H inside the grid
+  a.wg.half_h = win[1] % 2 == 0 ? 1 : 0;
+  if (a.wg.half_h) {
+    const int32_t half_win[3] = {win[0], win[1] / 2, win[2]};
+    if (!make_window_map(&a.tmap_q2, q, grid, half_win, 2 * frames, num_heads, head_dim) ||
+        !make_window_map(&a.tmap_k2, k, grid, half_win, 2 * frames, num_heads, head_dim) ||
+        !make_window_map(&a.tmap_v2, v, grid, half_win, 2 * frames, num_heads, head_dim))
+      return H3_ERR_CUDA;
+  }
   a.o = o;
   a.lse = lse;
   a.capacity = static_cast<int>(n);  // LSE row stride: [heads, T*H*W]
