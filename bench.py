@@ -43,6 +43,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--workload", default="h3_full_request",
                    choices=["h3_full_request", "single_request_4k", "continuation_batch",
+                            "continuation_batch_4seg",
                             "video_segment_16k", "window_grid", "window_grid_16x24x84",
                             "vsa_video", "vsa_video_16x24x84", "continuation_window", "tiny_example"],
                    help="h3_full_request is the metric's workload; the others are side measurements")

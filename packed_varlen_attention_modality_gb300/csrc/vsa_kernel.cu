@@ -14,11 +14,10 @@
 //                      8 x 8 register micro-tiles (two broadcast and two float4 shared loads per
 //                      64 FFMA), written to the caller's [H, nblk, nblk] score buffer
 //   vsa_topk_kernel    one warp per (head, query block): 8-bit radix select of the k-th largest
-//                      score over 4 passes (the row stays in L2), then an ascending ballot
+//                      score over 4 passes (the row stays in L1/L2), then an ascending ballot
 //                      compaction that takes the ties at the threshold lowest id first
 #include <cuda_bf16.h>
 
-#include <algorithm>
 #include <cstdint>
 
 #include "h3_internal.h"
@@ -31,7 +30,6 @@ constexpr int kScoreRows = 64;     // query blocks per score tile
 constexpr int kScoreCols = 256;    // key blocks per score tile
 constexpr int kScoreThreads = 256;
 constexpr int kTopkWarps = 8;
-constexpr size_t kTopkStageBytes = 200 * 1024;  // shared memory for staged score rows
 
 // Block b of the grid: origin and extent (cropped by the grid edge).
 struct BlockBox {
@@ -150,25 +148,18 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// One warp per (head, query block) row of the score matrix.  With `stage` set, each warp first
-// copies its row into shared memory (blockDim.x / 32 rows of nblk floats, dynamic) and runs the
-// five passes there; otherwise they re-read the row from global memory.
+// One warp per (head, query block) row of the score matrix.  The five passes re-read the row
+// (8 KB at 2016 blocks) through L1/L2: with only the 8 KB histogram in shared memory, enough
+// warps stay resident to hide the latency (staging rows in shared memory was slower).
 __global__ void __launch_bounds__(kTopkWarps * 32)
 vsa_topk_kernel(const float* __restrict__ scores, int rows, int nblk, int topk,
-                int32_t* __restrict__ sel, int stage) {
-  extern __shared__ float topk_rows[];
+                int32_t* __restrict__ sel) {
   __shared__ uint32_t hist_all[kTopkWarps][256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (blockDim.x >> 5) + warp;
+  const int row = blockIdx.x * kTopkWarps + warp;
   if (row >= rows) return;
   uint32_t* hist = hist_all[warp];
   const float* s = scores + static_cast<size_t>(row) * nblk;
-  if (stage) {
-    float* mine = topk_rows + static_cast<size_t>(warp) * nblk;
-    for (int i = lane; i < nblk; i += 32) mine[i] = s[i];
-    __syncwarp();
-    s = mine;
-  }
   // radix select of the topk-th largest key, 8 bits per pass from the top
   uint32_t prefix = 0, mask = 0;
   int remaining = topk;  // how many of the wanted keys still lie at or below the current prefix
@@ -235,21 +226,6 @@ vsa_topk_kernel(const float* __restrict__ scores, int rows, int nblk, int topk,
   }
 }
 
-cudaError_t configure_topk() {
-  static bool configured[64] = {};  // the shared-memory opt-in is made once per device
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(vsa_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kTopkStageBytes));
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
-  return cudaSuccess;
-}
-
 template <int D>
 cudaError_t launch_score(dim3 grid, const float* qm, const float* km, int nblk, float scale,
                          float* scores, cudaStream_t stream) {
@@ -293,16 +269,8 @@ cudaError_t launch_vsa_select(const void* q, const void* k, const VsaGeom& g, in
                       : launch_score<64>(sgrid, qm, km, nblk, scale, scores, stream);
   if (e != cudaSuccess) return e;
   const int rows = heads * nblk;
-  // rows staged in shared memory when at least one fits in the opt-in budget
-  const size_t row_bytes = static_cast<size_t>(nblk) * sizeof(float);
-  const int warps = static_cast<int>(std::min<size_t>(kTopkWarps, kTopkStageBytes / row_bytes));
-  const int stage = warps >= 1 ? 1 : 0;
-  const int per_cta = stage ? warps : kTopkWarps;
-  e = configure_topk();
-  if (e != cudaSuccess) return e;
-  vsa_topk_kernel<<<(rows + per_cta - 1) / per_cta, per_cta * 32,
-                    stage ? static_cast<size_t>(per_cta) * row_bytes : 0, stream>>>(
-      scores, rows, nblk, topk, sel, stage);
+  vsa_topk_kernel<<<(rows + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, stream>>>(
+      scores, rows, nblk, topk, sel);
   return cudaGetLastError();
 }
 

@@ -87,6 +87,7 @@ PACKED = {
     "tiny_example": lambda: W.tiny_example(capacity=64),
     "single_request_4k": lambda: W.single_request_4k(capacity=4160),
     "continuation_batch": lambda: W.continuation_batch(),
+    "continuation_batch_4seg": lambda: W.continuation_batch(per_request_segments=True),
     "h3_full_request": lambda: W.h3_full_request(),
 }
 FULL_CHECK = {"tiny_example", "single_request_4k"}
@@ -126,32 +127,34 @@ def test_attention_parity_on_gpu_rope_output(packed_case):
 
 
 def test_end_to_end_parity_from_raw_qk(packed_case):
-    """Parity (iii): the oracle does its own fp64 RoPE (with the time shift) from raw Q/K."""
+    """Parity (iii): the oracle does its own fp64 RoPE (with the time shift) from raw Q/K.  Short
+    segments are checked in full; long ones (sampled cases) on their sampled query rows, against
+    every key of the segment."""
     name, r = packed_case
     wl = r["wl"]
-    if not r["full"]:
-        # sampled rows need every key of their segment: restrict to the short segments + a slice
-        segs = [g for g in range(wl.num_segments) if wl.cu_seqlens[g + 1] - wl.cu_seqlens[g] <= 4096]
-        if not segs:
-            pytest.skip("no short segment to check end to end at this size")
-    else:
-        segs = list(range(wl.num_segments))
-    for g in segs:
+    for g in range(wl.num_segments):
         a, b = int(wl.cu_seqlens[g]), int(wl.cu_seqlens[g + 1])
+        if b <= a:
+            continue
         idx = np.arange(a, b)
+        if r["full"] or b - a <= 4096:
+            local = np.arange(b - a)
+        else:
+            local = r["rows"][(r["rows"] >= a) & (r["rows"] < b)] - a
         qo = oracle.rope_apply(wl.q, wl.pos, wl.tag, wl.cu_requests, wl.start_frames, rows=idx)
         ko = oracle.rope_apply(wl.k, wl.pos, wl.tag, wl.cu_requests, wl.start_frames, rows=idx)
         vo = wl.v[a:b].double().numpy()
-        ref_o, ref_lse = oracle.varlen_attention(qo, ko, vo, [0, b - a])
-        _close(r["o"][a:b].float().numpy(), ref_o, f"{name} e2e seg {g}")
+        ref_o, ref_lse = oracle.varlen_attention(qo, ko, vo, [0, b - a], rows=local)
+        _close(r["o"][a:b].float().numpy()[local], ref_o[local], f"{name} e2e seg {g}")
         # The GPU rounds the rotated Q/K to bf16 (storage) before attention.  Since
         # |d lse_i / d S_ij| = P_ij, |lse error| <= max_j |S_ij error| <=
         # scale * 2^-8 * max_j sum_d |q_id||k_jd| (two roundings of at most 2^-9 each).
         scale = 1.0 / np.sqrt(wl.head_dim)
-        aq, ak = np.abs(qo).transpose(1, 0, 2), np.abs(ko).transpose(1, 0, 2)  # [H, n, D]
+        aq, ak = np.abs(qo[local]).transpose(1, 0, 2), np.abs(ko).transpose(1, 0, 2)  # [H, n, D]
         bound = scale * 2.0 ** -8 * np.matmul(aq, ak.transpose(0, 2, 1)).max(axis=2)
-        got = r["lse"][:, a:b].numpy().astype(np.float64)
-        assert np.all(np.abs(got - ref_lse) <= bound + LSE_REL * np.maximum(np.abs(ref_lse), 1.0)), \
+        got = r["lse"][:, a:b].numpy().astype(np.float64)[:, local]
+        ref = ref_lse[:, local]
+        assert np.all(np.abs(got - ref) <= bound + LSE_REL * np.maximum(np.abs(ref), 1.0)), \
             f"{name} e2e seg {g}: lse outside the bf16-rounding bound"
 
 

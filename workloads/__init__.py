@@ -295,6 +295,7 @@ WORKLOADS = {
     "single_request_4k": single_request_4k,
     "h3_full_request": h3_full_request,
     "continuation_batch": continuation_batch,
+    "continuation_batch_4seg": lambda: continuation_batch(per_request_segments=True),
     "window_grid": window_grid,
     "video_segment_16k": video_segment_16k,
     "vsa_video": vsa_video,
