@@ -40,13 +40,15 @@
 //              when the running max grows by more than 2^8; the epilogue normalises O and
 //              stores it (and the LSE).
 //   warp 8     scheduler + TMA producer: Q tiles once per item, then K and V tiles through
-//              rings (3 K / 2 V stages at D = 128) that run on across items.
+//              rings that run on across items (at D = 128: 3 K / 2 V stages for packed
+//              segments, 2 K / 3 V for the grid variants).
 //   warp 9     MMA issuer (one thread).  Order per key tile j:
 //                PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
 //              so while softmax 0 works on S0_{j+1} the tensor core runs PV1_j and S1_{j+1},
 //              and vice versa (ping-pong).  Because S_t,{j+1} is issued after PV_t,j, seeing
 //              S_t,{j+1} complete also means O_t is stable for an in-place rescale.
-//   warps 10-11 idle (they complete warpgroup 2).
+//   warp 10    VSA only: TMA producer of the V tiles (the K tiles stay with warp 8).
+//   warp 11    idle (it completes warpgroup 2).
 // TMEM (512 columns): O0 [0,128), O1 [128,256), S0/P0 [256,384), S1/P1 [384,512).
 //
 // Barrier phases run on across items: every role counts its own completions and derives each
