@@ -367,7 +367,8 @@ def test_window_attention_in_place_matches_oracle_and_packed_path(h3, dev, windo
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("grid,win,shift", [((5, 9, 11), (4, 8, 8), (2, 4, 4)),
                                             ((3, 16, 8), (2, 8, 8), (1, 4, 0)),
-                                            ((6, 7, 5), (4, 4, 8), (0, 2, 3))])
+                                            ((6, 7, 5), (4, 4, 8), (0, 2, 3)),
+                                            ((7, 9, 20), (3, 4, 16), (1, 2, 8))])
 def test_window_attention_in_place_small_grids_full_oracle(h3, dev, D, grid, win, shift):
     n = grid[0] * grid[1] * grid[2]
     rng = np.random.default_rng(n + D)

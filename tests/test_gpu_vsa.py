@@ -218,3 +218,23 @@ def test_video_grid_at_bench_size_sampled(h3, dev):
     got = o.float().cpu().numpy()[:, heads]
     _close(got[rows], ref_o[rows], "vsa 32x48x84 sampled")
     _lse_close(lse.cpu().numpy()[heads][:, rows], ref_lse[:, rows], "vsa 32x48x84 sampled")
+
+
+@pytest.mark.parametrize("block", [(2, 4, 8), (8, 2, 4)])
+def test_non_cubic_64_token_blocks(h3, dev, block):
+    """The block shape is the caller's as long as it holds 64 tokens: selection and attention
+    with 2x4x8 and 8x2x4 blocks on a grid cropped on every axis."""
+    grid, D, H = (9, 10, 13), 64, 2
+    n = grid[0] * grid[1] * grid[2]
+    q, k, v = _qkv(17 + block[0], n, H, D)
+    nblk = oracle.vsa_block_count(grid, block)
+    topk = min(4, nblk)
+    sel, scores = h3.vsa_select(q.to(dev), k.to(dev), grid, topk, block=block)
+    o, lse = h3.vsa_attn_fwd(q.to(dev), k.to(dev), v.to(dev), grid, sel, block=block, return_lse=True)
+    torch.cuda.synchronize()
+    assert h3.get_device_error(dev) == 0
+    sel_np = sel.cpu().numpy()
+    _check_selection(sel_np, scores.cpu().numpy(), q, k, grid, block, topk, D)
+    ref_o, ref_lse = oracle.vsa_attention(q, k, v, grid, block, sel_np)
+    _close(o.float().cpu().numpy(), ref_o, f"vsa block {block}")
+    _lse_close(lse.cpu().numpy(), ref_lse, f"vsa block {block}")
