@@ -170,7 +170,12 @@ def test_pad_rows_of_output_untouched(h3, dev):
 
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("lengths", [[1, 127, 128, 129, 0, 255, 256, 257, 2, 383],
-                                     [1000, 1, 1, 513], [0, 0, 77], [128 * 5]])
+                                     [1000, 1, 1, 513], [0, 0, 77], [128 * 5],
+                                     # the grid switches from one CTA per SM (max_seqlen <= 2048)
+                                     # to one CTA per item just above it
+                                     [2048, 5, 0], [2049, 300, 1],
+                                     # more segments than the plan orders longest-first (256)
+                                     [int(x) for x in np.random.default_rng(23).integers(0, 40, 300)]])
 def test_edge_lengths_against_oracle(h3, dev, D, lengths):
     wl = W.random_packed(100 + sum(lengths) % 97, lengths, heads=3, head_dim=D,
                          capacity=sum(lengths) + 61)
