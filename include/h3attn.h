@@ -376,6 +376,12 @@ H3_API h3_status h3_sp_assign_windows(const int32_t grid[3], const int32_t win[3
                                       const int32_t shift[3], int32_t world, int32_t* window_rank,
                                       int64_t* rank_tokens);
 
+/* Tokens each rank owns under a window -> rank map of one layer.
+ * rank_tokens: int64 [world] out.  Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG. */
+H3_API h3_status h3_sp_rank_tokens(const int32_t grid[3], const int32_t win[3],
+                                   const int32_t shift[3], const int32_t* window_rank,
+                                   int32_t world, int64_t* rank_tokens);
+
 /* A rank's local row order in one layer: the original (row-major) index of each token it owns,
  * its windows ascending and tokens row-major inside (the single-GPU packed order restricted to
  * the rank).  order: int32 [rank_tokens[rank]] out (order_capacity entries available).

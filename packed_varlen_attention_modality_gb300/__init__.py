@@ -14,10 +14,10 @@ Calls:
                     selection, then attention over the selected 64-token blocks
   continuation_plan / continuation_pack / continuation_append / masked_row_update
                     continuation window: tails, five row groups, overlap discard, target updates
-  sp_assign_windows / sp_layer_order / sp_exchange_plan / sp_exchange
-                    window-aligned sequence parallelism: window owners, local orders, the
-                    all-to-all of a regular <-> shifted switch (planning native, rows moved by
-                    torch.distributed)
+  sp_assign_windows / sp_rank_tokens / sp_layer_order / sp_exchange_plan
+                    window-aligned sequence parallelism: window owners, local orders and the
+                    all-to-all plan of a regular <-> shifted switch (host planning; the caller
+                    moves the rows with its own all-to-all)
   get_device_error  read (and clear) the device-side error word
 """
 from __future__ import annotations
@@ -33,7 +33,7 @@ __all__ = ["H3Error", "RopeConfig", "lib_path", "load_library", "rope_apply", "v
            "vsa_select_workspace_size", "vsa_select", "vsa_attn_fwd", "ContinuationConfig",
            "ContinuationPlan", "continuation_config", "continuation_plan", "continuation_pack",
            "continuation_append", "masked_row_update", "sp_assign_windows", "sp_layer_order",
-           "sp_rank_tokens", "sp_exchange_plan", "sp_exchange",
+           "sp_rank_tokens", "sp_exchange_plan",
            "varlen_attn_workspace_size", "window_count", "window_pack", "window_unpack",
            "get_device_error", "TAG_TEXT", "TAG_VIDEO", "TAG_AUDIO"]
 
@@ -115,6 +115,7 @@ def load_library():
                                          ctypes.c_int64, P]),
         "h3_masked_row_update": (I32, [P, P, P, I32, I32, P]),
         "h3_sp_assign_windows": (I32, [I32P, I32P, I32P, I32, P, P]),
+        "h3_sp_rank_tokens": (I32, [I32P, I32P, I32P, P, I32, P]),
         "h3_sp_layer_order": (I32, [I32P, I32P, I32P, P, I32, I32, P, ctypes.c_int64]),
         "h3_sp_exchange_plan": (I32, [I32P, I32P, I32P, P, I32P, P, I32, I32, P, P, P, P]),
         "h3_vsa_select_workspace_size": (U64, [I32P, I32P, I32, I32]),
@@ -596,13 +597,11 @@ def sp_rank_tokens(grid, win, shift, window_rank, world: int):
     """Tokens each rank owns under a given window -> rank map (numpy int64 [world])."""
     import numpy as np
 
-    owner = np.asarray(window_rank, dtype=np.int64)
-    sizes = np.empty(owner.size, np.int64)
-    nw = [(int(L) + int(s) + int(w) - 1) // int(w) for L, w, s in zip(grid, win, shift)]
-    axes = [np.array([min(L, (i + 1) * w - s) - max(0, i * w - s) for i in range(n)])
-            for L, w, s, n in zip(grid, win, shift, nw)]
-    sizes[:] = np.einsum("i,j,k->ijk", *axes).reshape(-1)
-    return np.bincount(owner, weights=sizes, minlength=int(world)).astype(np.int64)
+    owner = np.ascontiguousarray(window_rank, dtype=np.int32)
+    tokens = np.empty(int(world), dtype=np.int64)
+    _check(load_library().h3_sp_rank_tokens(_i3(grid), _i3(win), _i3(shift), _np_ptr(owner), int(world),
+                                            _np_ptr(tokens)), "h3_sp_rank_tokens")
+    return tokens
 
 
 def sp_exchange_plan(grid, win, shift_from, rank_from, shift_to, rank_to, world: int, rank: int):
@@ -624,22 +623,6 @@ def sp_exchange_plan(grid, win, shift_from, rank_from, shift_to, rank_to, world:
     plan["send_index"] = plan["send_index"][:n_from]
     plan["recv_position"] = plan["recv_position"][:n_to]
     return plan
-
-
-def sp_exchange(x_local: torch.Tensor, plan, group=None) -> torch.Tensor:
-    """Move a rank's rows from its `from` layout to its `to` layout: gather by the plan's send
-    index, one all_to_all_single, scatter to the receive positions (torch.distributed)."""
-    import torch.distributed as dist
-
-    dev = x_local.device
-    send = x_local.index_select(0, torch.from_numpy(plan["send_index"]).long().to(dev))
-    n_to = int(plan["recv_counts"].sum())
-    recv = torch.empty((n_to,) + tuple(x_local.shape[1:]), dtype=x_local.dtype, device=dev)
-    dist.all_to_all_single(recv, send, output_split_sizes=[int(c) for c in plan["recv_counts"]],
-                           input_split_sizes=[int(c) for c in plan["send_counts"]], group=group)
-    out = torch.empty_like(recv)
-    out[torch.from_numpy(plan["recv_position"]).long().to(dev)] = recv
-    return out
 
 
 def get_device_error(device: Optional[torch.device] = None) -> int:

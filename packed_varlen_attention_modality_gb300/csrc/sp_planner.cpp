@@ -125,6 +125,19 @@ h3_status h3_sp_assign_windows(const int32_t grid[3], const int32_t win[3], cons
   return H3_OK;
 }
 
+h3_status h3_sp_rank_tokens(const int32_t grid[3], const int32_t win[3], const int32_t shift[3],
+                            const int32_t* window_rank, int32_t world, int64_t* rank_tokens) {
+  if (grid == nullptr || win == nullptr || shift == nullptr || window_rank == nullptr ||
+      rank_tokens == nullptr)
+    return H3_ERR_NULL;
+  const Layer g(grid, win, shift);
+  if (!g.ok || world <= 0) return H3_ERR_INVALID_ARG;
+  if (!ranks_valid(window_rank, g.windows(), world)) return H3_ERR_INVALID_ARG;
+  std::fill(rank_tokens, rank_tokens + world, 0);
+  for (int32_t i = 0; i < g.windows(); ++i) rank_tokens[window_rank[i]] += g.size_of(i);
+  return H3_OK;
+}
+
 h3_status h3_sp_layer_order(const int32_t grid[3], const int32_t win[3], const int32_t shift[3],
                             const int32_t* window_rank, int32_t world, int32_t rank,
                             int32_t* order, int64_t order_capacity) {
