@@ -46,7 +46,10 @@
 //                PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
 //              so while softmax 0 works on S0_{j+1} the tensor core runs PV1_j and S1_{j+1},
 //              and vice versa (ping-pong).  Because S_t,{j+1} is issued after PV_t,j, seeing
-//              S_t,{j+1} complete also means O_t is stable for an in-place rescale.
+//              S_t,{j+1} complete also means O_t is stable for an in-place rescale.  In the
+//              packed and window variants the softmax publishes P over the first 64 keys on
+//              its own barrier, and PV_t,j runs as two halves of 64 keys, the first while the
+//              softmax still exponentiates the second half of the row.
 //   warp 10    VSA only: TMA producer of the V tiles (the K tiles stay with warp 8).
 //   warp 11    idle (it completes warpgroup 2).
 // TMEM (512 columns): O0 [0,128), O1 [128,256), S0/P0 [256,384), S1/P1 [384,512).
@@ -342,8 +345,8 @@ struct Cfg {
   static constexpr int kStagesK = (D == 128) ? (kMode == kModePacked ? 3 : 2) : 4;
   static constexpr int kStagesV = (D == 128) ? (kMode == kModePacked ? 2 : 3) : 4;
   // q_full[2], q_empty, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
-  // p_full[2], o_final[2], o_empty[2], w_full[2], w_empty[2], drain
-  static constexpr int kNumBars = 3 + 2 * kStagesK + 2 * kStagesV + 12 + 1;
+  // p_full[2], o_final[2], o_empty[2], w_full[2], w_empty[2], drain, p_half[2]
+  static constexpr int kNumBars = 3 + 2 * kStagesK + 2 * kStagesV + 12 + 1 + 2;
   static constexpr int kSmemBytes = 1024 /*alignment slack*/ +
                                     kTileBytes * (kTilesPerItem + kStagesK + kStagesV) +
                                     kNumBars * 8 + 16 /*TMEM slot*/ + 2 * sizeof(WorkDesc);
@@ -426,6 +429,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
   auto bar_wfull = [&](int i) { return smem_u32(&bars[kB + 8 + i]); };
   auto bar_wempty = [&](int i) { return smem_u32(&bars[kB + 10 + i]); };
   const uint32_t bar_drain = smem_u32(&bars[kB + 12]);
+  // P_t over the first 64 keys written (packed and window variants)
+  auto bar_phalf = [&](int t) { return smem_u32(&bars[kB + 13 + t]); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -448,6 +453,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       mbar_init(bar_qfull(t), 1);
       mbar_init(bar_sfull(t), 1);
       mbar_init(bar_pfull(t), 128);
+      mbar_init(bar_phalf(t), 128);
       mbar_init(bar_ofinal(t), 1);
       mbar_init(bar_oempty(t), 128);
       mbar_init(bar_wfull(t), 1);
@@ -644,11 +650,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
         mma_commit(bar_sfull(t));
       };
-      auto issue_pv = [&](int t, int s, bool first) {  // O_t += P_t V_s
+      // O_t += P_t V_s over keys [16 kk0, 16 kk1) of the tile
+      auto issue_pv = [&](int t, int s, bool first, int kk0 = 0, int kk1 = kBlockN / 16) {
         const uint32_t p = tmem + kColS + 128 * t;
         const uint32_t vlo = dv.lo + s * kTile16;
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
+        for (int kk = kk0; kk < kk1; ++kk)
           // 16 keys per MMA: 8 TMEM columns of packed bf16 P; 16 rows (2 KB) of V
           mma_ts_split(tmem + kColO + 128 * t, p + kk * 8, vlo + kk * (2048 >> 4), dv.hi,
                        C::kIdescPV, (!first || kk > 0) ? 1u : 0u);
@@ -753,14 +760,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
             fence_proxy_async_smem();
             __syncwarp();
           }
-          // tile 0: PV0_j (the item's first one waits for the previous epilogue), then S0_{j+1}
-          ok = wait_all(bar_pfull(0), pn[0]++ & 1);
+          // tile 0: PV0_j (the item's first one waits for the previous epilogue), then S0_{j+1}.
+          // PV runs in two halves of 64 keys: the first starts as soon as the softmax has
+          // written P over those keys, while it still works on the other half.
+          ok = wait_all(bar_phalf(0), pn[0] & 1);
           if (ok && j == 0) ok = wait_all(bar_oempty(0), (un[0] & 1) ^ 1);
+          if (!ok) break;
+          tc_fence_after();
+          if (leader) issue_pv(0, sv, j == 0, 0, kBlockN / 32);
+          __syncwarp();
+          ok = wait_all(bar_pfull(0), pn[0]++ & 1);
           if (ok && more) ok = wait_all(bar_kfull(sk), (kc / SK) & 1);
           if (!ok) break;
           tc_fence_after();
           if (leader) {
-            issue_pv(0, sv, j == 0);
+            issue_pv(0, sv, j == 0, kBlockN / 32, kBlockN / 16);
             if (!more) mma_commit(bar_ofinal(0));
             if (more) issue_qk(0, sk);
             if (!has1) {
@@ -771,13 +785,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           }
           __syncwarp();
           if (has1) {
-            // tile 1: PV1_j, then S1_{j+1}
-            ok = wait_all(bar_pfull(1), pn[1]++ & 1);
+            // tile 1: PV1_j in two halves, then S1_{j+1}
+            ok = wait_all(bar_phalf(1), pn[1] & 1);
             if (ok && j == 0) ok = wait_all(bar_oempty(1), (un[1] & 1) ^ 1);
             if (!ok) break;
             tc_fence_after();
+            if (leader) issue_pv(1, sv, j == 0, 0, kBlockN / 32);
+            __syncwarp();
+            ok = wait_all(bar_pfull(1), pn[1]++ & 1);
+            if (!ok) break;
+            tc_fence_after();
             if (leader) {
-              issue_pv(1, sv, j == 0);
+              issue_pv(1, sv, j == 0, kBlockN / 32, kBlockN / 16);
               mma_commit(bar_vempty(sv));
               if (!more) mma_commit(bar_ofinal(1));
               if (more) {
@@ -983,8 +1002,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const float2 nm2 = make_float2(-mb, -mb);
         float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
         uint32_t p[64];
+        // P over keys 0-63 first, published on its own so PV can start on it
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < 32; ++c) {
+          const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), c2, nm2);
+          const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          acc[c & 3] = fadd2(acc[c & 3], e);
+          p[c] = pack_bf16x2(e.x, e.y);
+        }
+        tmem_st32(s_addr + 0, p + 0);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_phalf(t));
+#pragma unroll
+        for (int c = 32; c < 64; ++c) {
           const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), c2, nm2);
           const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           acc[c & 3] = fadd2(acc[c & 3], e);
@@ -993,7 +1024,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const float2 a01 = fadd2(acc[0], acc[1]);
         const float2 a23 = fadd2(acc[2], acc[3]);
         l += (a01.x + a01.y) + (a23.x + a23.y);
-        tmem_st32(s_addr + 0, p + 0);
         tmem_st32(s_addr + 32, p + 32);
         tmem_st_wait();
         tc_fence_before();
