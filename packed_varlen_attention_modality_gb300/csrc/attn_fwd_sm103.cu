@@ -41,7 +41,7 @@
 //              stores it (and the LSE).
 //   warp 8     scheduler + TMA producer: Q tiles once per item, then K and V tiles through
 //              rings that run on across items (at D = 128: 3 K / 2 V stages for packed
-//              segments, 2 K / 3 V for the grid variants).
+//              segments and VSA, 2 K / 3 V for windows).
 //   warp 9     MMA issuer (one thread).  Order per key tile j:
 //                PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
 //              so while softmax 0 works on S0_{j+1} the tensor core runs PV1_j and S1_{j+1},
@@ -338,12 +338,12 @@ struct Cfg {
   static constexpr int kBoxes = D / 64;               // 64-column (128-byte) swizzle boxes
   static constexpr int kTileBytes = kBlockM * D * 2;  // one Q, K or V tile
   static constexpr int kBoxBytes = kBlockM * 128;     // one 128-row box
-  // Ring depths (5 tiles of 32 KB fit beside the two Q tiles at D = 128).  Packed segments:
-  // 3 K + 2 V.  The grid variants: 2 K + 3 V -- a V tile is loaded only once the PV product two
-  // entries back has drained, so V gains most from depth (VSA, which takes a K and a V tile per
-  // query tile per step: 50 -> 39 ms on the 1344x768 latent; windows: 1-1.5 %).
-  static constexpr int kStagesK = (D == 128) ? (kMode == kModePacked ? 3 : 2) : 4;
-  static constexpr int kStagesV = (D == 128) ? (kMode == kModePacked ? 2 : 3) : 4;
+  // Ring depths (5 tiles of 32 KB fit beside the two Q tiles at D = 128).  Packed segments and
+  // VSA: 3 K + 2 V.  Windows: 2 K + 3 V (1-1.5 % faster there).  VSA takes a K and a V tile per
+  // query tile per step, so with one producer thread V gained most from depth (50 -> 39 ms on the
+  // 1344x768 latent); with V on its own producer thread, K does (34.9 -> 33.9 ms).
+  static constexpr int kStagesK = (D == 128) ? (kMode != kModeWindow ? 3 : 2) : 4;
+  static constexpr int kStagesV = (D == 128) ? (kMode != kModeWindow ? 2 : 3) : 4;
   // q_full[2], q_empty, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
   // p_full[2], o_final[2], o_empty[2], w_full[2], w_empty[2], drain, p_half[2]
   static constexpr int kNumBars = 3 + 2 * kStagesK + 2 * kStagesV + 12 + 1 + 2;
