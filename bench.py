@@ -36,7 +36,7 @@ L2_BYTES = 129 * 2 ** 20
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-e2e", action="store_true")
@@ -289,7 +289,8 @@ def run_ours(args, rank, world, local_rank):
     if h3.get_device_error(dev) != 0:
         raise RuntimeError("device error during the timed steps")
     rope_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
-    attn_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    attn_each = [e[1].elapsed_time(e[2]) for e in evs]
+    attn_ms = float(np.mean(attn_each))
     ms_per_step = total_ms / args.steps
     value = job_throughput(flops, world, ms_per_step)
 
@@ -331,7 +332,10 @@ def run_ours(args, rank, world, local_rank):
                          "attn_ms": attn_ms},
             "kernels": {"rope": {"ms": rope_ms, "gbs": rope_gbs, "bytes": rope_bytes,
                                  "frac_hbm": rope_gbs / peaks["hbm_gbs"]},
-                        "attn_fwd": {"ms": attn_ms, "tflops": attn_tflops}},
+                        "attn_fwd": {"ms": attn_ms, "tflops": attn_tflops,
+                                     "ms_median": float(np.median(attn_each)),
+                                     "ms_min": float(np.min(attn_each)),
+                                     "tflops_median": flops / (float(np.median(attn_each)) / 1e3) / 1e12}},
             "clocks": clocks,
             "gpu_launches": 3 * args.steps,   # RoPE, attention plan, attention per step
             "e2e": e2e,
