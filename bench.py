@@ -45,7 +45,8 @@ def parse_args():
                    choices=["h3_full_request", "single_request_4k", "continuation_batch",
                             "continuation_batch_4seg",
                             "video_segment_16k", "window_grid", "window_grid_16x24x84",
-                            "vsa_video", "vsa_video_16x24x84", "continuation_window", "tiny_example"],
+                            "vsa_video", "vsa_video_16x24x84", "vsa_video_shared_half", "continuation_window",
+                            "tiny_example"],
                    help="h3_full_request is the metric's workload; the others are side measurements")
     return p.parse_args()
 
@@ -549,8 +550,9 @@ def run_vsa(args, rank, world, dev, h3, peaks):
     """Block-sparse video attention on the 1344x768 latent (32x48x84 grid, 4x4x4 blocks = 2016,
     top 252 = 1/8; 24 heads x 128): per step the block gate + top-k selection, then the attention
     of every query block over its selected blocks.  vsa_video_16x24x84 is a quarter of the grid
-    for full ncu captures."""
-    from workloads import vsa_video
+    for full ncu captures.  vsa_video_shared_half times the attention alone over a fixed synthetic
+    selection in which paired query blocks share half of their 252 blocks (the gate is skipped)."""
+    from workloads import vsa_paired_selection, vsa_video
 
     wl = vsa_video(grid=(16, 24, 84), topk=126) if args.workload == "vsa_video_16x24x84" else vsa_video()
     n, H, D = wl.num_tokens, wl.num_heads, wl.head_dim
@@ -560,16 +562,23 @@ def run_vsa(args, rank, world, dev, h3, peaks):
     scores = torch.empty((H, nblk, nblk), dtype=torch.float32, device=dev)
     sel = torch.empty((H, nblk, wl.topk), dtype=torch.int32, device=dev)
     ws = torch.empty(h3.vsa_select_workspace_size(wl.grid, wl.block, H, D), dtype=torch.uint8, device=dev)
+    ws_attn = torch.empty(h3.vsa_attn_workspace_size(wl.grid, wl.block, H, wl.topk), dtype=torch.uint8,
+                          device=dev)
     o = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
+
+    fixed_sel = args.workload == "vsa_video_shared_half"
+    if fixed_sel:
+        sel.copy_(torch.from_numpy(vsa_paired_selection(9, H, nblk, wl.topk, wl.topk // 2)))
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        h3.vsa_select(q, k, wl.grid, wl.topk, block=wl.block, scores=scores, out=sel, workspace=ws)
+        if not fixed_sel:
+            h3.vsa_select(q, k, wl.grid, wl.topk, block=wl.block, scores=scores, out=sel, workspace=ws)
         if ev is not None:
             ev[1].record(stream)
-        h3.vsa_attn_fwd(q, k, v, wl.grid, sel, block=wl.block, out=o)
+        h3.vsa_attn_fwd(q, k, v, wl.grid, sel, block=wl.block, out=o, workspace=ws_attn)
         if ev is not None:
             ev[2].record(stream)
 
@@ -581,6 +590,17 @@ def run_vsa(args, rank, world, dev, h3, peaks):
     # useful attention FLOPs from the selection: 4 H D sum_a n_a sum_{b in sel(a)} n_b
     sizes = torch.tensor(_block_sizes(wl.grid, wl.block), dtype=torch.float64, device=dev)
     flops = float(4.0 * D * (sizes[None, :, None] * sizes[sel.long()]).sum().item())
+    # executed MMA work: query blocks 2p and 2p + 1 share a 128-row tile; a key block both of them
+    # selected serves both halves of a step, so a pair sharing s of its topk blocks runs
+    # ceil(s/2) + topk - s steps of a 128 x 128 QK^T and PV (the selection lists are distinct ids)
+    sel_np = sel.cpu().numpy()
+    first = sel_np[:, 0::2]
+    second = sel_np[:, 1::2] if nblk % 2 == 0 else np.concatenate([sel_np[:, 1::2], first[:, -1:]], axis=1)
+    member = np.zeros(second.shape[:2] + (nblk,), bool)
+    np.put_along_axis(member, second.astype(np.int64), True, axis=2)
+    shared = np.take_along_axis(member, first.astype(np.int64), axis=2).sum(axis=2)
+    steps = (shared + 1) // 2 + wl.topk - shared
+    flops_executed = float(steps.sum()) * 4.0 * 128 * 128 * D
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     sampler = ClockSampler(dev.index)
     torch.cuda.synchronize(dev)
@@ -601,7 +621,9 @@ def run_vsa(args, rank, world, dev, h3, peaks):
     attn_tflops = flops / attn_ms / 1e9
     if rank == 0:
         print(json.dumps({
-            "metric": "block-sparse video attention TFLOP/s (gate + top-k + attention over selected blocks)",
+            "metric": ("block-sparse video attention TFLOP/s (attention over a fixed selection: paired "
+                       "query blocks share half their blocks)" if fixed_sel else
+                       "block-sparse video attention TFLOP/s (gate + top-k + attention over selected blocks)"),
             "value": job_throughput(flops, world, ms_per_step), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -611,15 +633,18 @@ def run_vsa(args, rank, world, dev, h3, peaks):
                        "l2": "inputs larger than L2 (%d MB per tensor)" % round(n * H * D * 2 / 1e6)},
             "kernels": {"select": {"ms": sel_ms, "note": "block means + fp32 score GEMM + radix top-k"},
                         "attn": {"ms": attn_ms, "tflops_useful": attn_tflops,
-                                 "tflops_executed": 2 * attn_tflops,
-                                 "note": "each 128-row tile holds two query blocks with their own key "
-                                         "blocks: half of every MMA is masked work"}},
+                                 "tflops_executed": flops_executed / attn_ms / 1e9,
+                                 "shared_selection_frac": float(shared.mean() / wl.topk),
+                                 "steps": int(steps.sum()), "steps_unshared": int(steps.size * wl.topk),
+                                 "note": "each 128-row tile holds two query blocks; a step stacks two "
+                                         "key blocks, and a block selected by only one of them is "
+                                         "masked for the other half"}},
             "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": attn_tflops / peaks["bf16_tflops"], "traffic": None,
                          "kernel": "attn_fwd_kernel<%d, vsa>" % D,
                          "peak_source": peaks["source"] + " bf16_tflops (burst)",
                          "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"]},
-            "clocks": clocks, "gpu_launches": 4 * args.steps}), flush=True)
+            "clocks": clocks, "gpu_launches": (2 if fixed_sel else 5) * args.steps}), flush=True)
 
 
 def run_continuation(args, rank, world, dev, h3, peaks):

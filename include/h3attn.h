@@ -271,6 +271,10 @@ H3_API h3_status h3_vsa_select(const void* q, const void* k, const int32_t grid[
                                int32_t topk, float softmax_scale, float* scores, int32_t* block_idx,
                                void* workspace, size_t workspace_bytes, h3_stream_t stream);
 
+/* Workspace bytes of h3_vsa_attn_fwd (the key/value schedule); 0 for invalid sizes. */
+H3_API size_t h3_vsa_attn_workspace_size(const int32_t grid[3], const int32_t block[3],
+                                         int32_t num_heads, int32_t topk);
+
 /* Token-level attention over the selected blocks: query i of block a attends, with one softmax,
  * to every key row of the blocks block_idx[h][a][0..topk) (rows inside the grid only).
  * q, k, v, o : device bf16 [T*H*W, num_heads, head_dim] (layout above); o gets every row.
@@ -278,13 +282,20 @@ H3_API h3_status h3_vsa_select(const void* q, const void* k, const int32_t grid[
  * block_idx  : device int32 [num_heads, nblk, topk], e.g. from h3_vsa_select; any order, ids
  *              distinct per list (a repeated id counts its keys twice).  An id outside [0, nblk)
  *              is replaced by block 0 and recorded as H3_ERR_BAD_BLOCK_INDEX.
- * softmax_scale: <= 0 selects 1/sqrt(head_dim).  No workspace.
- * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG, H3_ERR_UNSUPPORTED, H3_ERR_MISALIGNED, H3_ERR_CUDA;
- *         device-side H3_ERR_BAD_BLOCK_INDEX / H3_ERR_TIMEOUT. */
+ * softmax_scale: <= 0 selects 1/sqrt(head_dim).
+ * workspace  : device, >= h3_vsa_attn_workspace_size() bytes, 16-byte aligned; overwritten.
+ * Query blocks 2p and 2p + 1 share a 128-row tile, and each step of the tile loads two key blocks.
+ * A first kernel writes each pair's steps into the workspace. When both lists are in ascending
+ * order (as h3_vsa_select writes them), a block both query blocks selected serves both in one
+ * step, so a pair sharing s blocks takes ceil(s/2) + topk - s steps instead of topk. Lists in any
+ * other order take topk steps. The result is the same either way, up to summation order.
+ * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG, H3_ERR_UNSUPPORTED, H3_ERR_WORKSPACE,
+ *         H3_ERR_MISALIGNED, H3_ERR_CUDA; device-side H3_ERR_BAD_BLOCK_INDEX / H3_ERR_TIMEOUT. */
 H3_API h3_status h3_vsa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                                  const int32_t grid[3], const int32_t block[3], int32_t num_heads,
                                  int32_t head_dim, const int32_t* block_idx, int32_t topk,
-                                 float softmax_scale, h3_stream_t stream);
+                                 float softmax_scale, void* workspace, size_t workspace_bytes,
+                                 h3_stream_t stream);
 
 /* ---- Continuation window ---------------------------------------------------------------------
  * [H3-fast] "Breaking the engineering bottlenecks of video-generation models", section "Crossing

@@ -30,7 +30,8 @@ import torch
 
 __all__ = ["H3Error", "RopeConfig", "lib_path", "load_library", "rope_apply", "varlen_attn_fwd",
            "varlen_attn_fwd_noalloc", "window_attn_fwd", "vsa_block_count",
-           "vsa_select_workspace_size", "vsa_select", "vsa_attn_fwd", "ContinuationConfig",
+           "vsa_select_workspace_size", "vsa_select", "vsa_attn_workspace_size", "vsa_attn_fwd",
+           "ContinuationConfig",
            "ContinuationPlan", "continuation_config", "continuation_plan", "continuation_pack",
            "continuation_append", "masked_row_update", "sp_assign_windows", "sp_layer_order",
            "sp_rank_tokens", "sp_exchange_plan",
@@ -120,7 +121,8 @@ def load_library():
         "h3_sp_exchange_plan": (I32, [I32P, I32P, I32P, P, I32P, P, I32, I32, P, P, P, P]),
         "h3_vsa_select_workspace_size": (U64, [I32P, I32P, I32, I32]),
         "h3_vsa_select": (I32, [P, P, I32P, I32P, I32, I32, I32, F32, P, P, P, U64, P]),
-        "h3_vsa_attn_fwd": (I32, [P, P, P, P, P, I32P, I32P, I32, I32, P, I32, F32, P]),
+        "h3_vsa_attn_workspace_size": (U64, [I32P, I32P, I32, I32]),
+        "h3_vsa_attn_fwd": (I32, [P, P, P, P, P, I32P, I32P, I32, I32, P, I32, F32, P, U64, P]),
         "h3_get_device_error": (I32, [P]),
         "h3_status_string": (ctypes.c_char_p, [I32]),
         "h3_version": (I32, []),
@@ -443,14 +445,21 @@ def vsa_select(q: torch.Tensor, k: torch.Tensor, grid: Sequence[int], topk: int,
     return out, scores
 
 
+def vsa_attn_workspace_size(grid: Sequence[int], block: Sequence[int], num_heads: int,
+                            topk: int) -> int:
+    return int(load_library().h3_vsa_attn_workspace_size(_i3(grid), _i3(block), num_heads, topk))
+
+
 def vsa_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grid: Sequence[int],
                  block_idx: torch.Tensor, block: Sequence[int] = (4, 4, 4),
                  out: Optional[torch.Tensor] = None, return_lse: bool = False,
-                 lse: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None):
+                 lse: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None,
+                 workspace: Optional[torch.Tensor] = None):
     """Token-level attention of every query block over its selected key blocks (VSA).
 
     q, k, v: bf16 [T*H*W, heads, D] in row-major (t, h, w) order; block_idx int32
-    [heads, nblk, topk].  Returns out (and lse fp32 [heads, T*H*W] when requested).
+    [heads, nblk, topk]; workspace uint8 of vsa_attn_workspace_size() bytes (allocated when
+    omitted).  Returns out (and lse fp32 [heads, T*H*W] when requested).
     """
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -475,10 +484,15 @@ def vsa_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grid: Sequen
         if tuple(lse.shape) != (H, n):
             raise ValueError("lse must be [heads, T*H*W]")
     scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    need = vsa_attn_workspace_size(grid, block, H, topk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _require(workspace, "workspace", torch.uint8, dev)
     lib = load_library()
     with torch.cuda.device(dev):
         st = lib.h3_vsa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _i3(grid),
-                                 _i3(block), H, D, _ptr(block_idx), topk, scale, _stream(dev))
+                                 _i3(block), H, D, _ptr(block_idx), topk, scale, _ptr(workspace),
+                                 workspace.numel(), _stream(dev))
     _check(st, "h3_vsa_attn_fwd")
     return (out, lse) if (return_lse or lse is not None) else out
 

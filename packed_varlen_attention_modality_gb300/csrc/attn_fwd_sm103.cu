@@ -100,7 +100,9 @@ struct WorkDesc {
   int q0;         // packed: first query row of the item
   int box[3];     // window: grid (t, h, w) of the first valid tile's box origin (may be < 0)
   int ntiles;     // window / VSA: query tiles of the item (1 or 2)
-  int nkv;        // window / VSA: key/value steps of the item
+  int nkv;        // window / VSA: key/value steps of the item (VSA: the larger tile's)
+  int nkv_t[2];   // VSA: key/value steps of each query tile
+  int nsh_t[2];   // VSA: key blocks both query blocks of the tile selected
   int hbox;       // window: box rows along H (the window's, or half of it for an edge window)
   int fpt;        // window: frames per 128-row tile (128 / (hbox * window W))
   uint32_t mask[2][4];  // window: rows of each tile that lie inside the grid (= inside the window)
@@ -214,31 +216,32 @@ __device__ __forceinline__ uint64_t vsa_block_mask(int b, const WindowAttnGeom& 
   return m;
 }
 // Item -> descriptor: query blocks q0 .. q0 + 3 of one head (tile t holds blocks q0 + 2t and
-// q0 + 2t + 1 in its two 64-row halves).  Items are numbered head-major: the CTAs working at one
-// time serve one head (two at a boundary), so the key/value blocks they select at random stay
-// in L2 (one head's K and V of the 32x48x84 grid are 66 MB), instead of every head's at once.
+// q0 + 2t + 1 in its two 64-row halves: pair q0 / 2 + t of the key/value schedule).  Items are
+// numbered head-major: the CTAs working at one time serve one head (two at a boundary), so the
+// key/value blocks they select at random stay in L2 (one head's K and V of the 32x48x84 grid
+// are 66 MB), instead of every head's at once.
 __device__ __forceinline__ WorkDesc decode_vsa(uint32_t item, const WindowAttnGeom& g,
-                                               int num_heads) {
+                                               const int2* __restrict__ counts) {
   WorkDesc d{};
   d.seg_len = 1;
-  const uint32_t quads = static_cast<uint32_t>((vsa_num_blocks(g) + 3) / 4);
+  const int nblk = vsa_num_blocks(g);
+  const uint32_t quads = static_cast<uint32_t>((nblk + 3) / 4);
   d.head = static_cast<int>(item / quads);
   d.q0 = 4 * static_cast<int>(item % quads);
-  (void)num_heads;
-  d.ntiles = d.q0 + 2 < vsa_num_blocks(g) ? 2 : 1;
-  d.nkv = g.topk;
+  d.ntiles = d.q0 + 2 < nblk ? 2 : 1;
+  const int2* c = counts + static_cast<size_t>(d.head) * ((nblk + 1) / 2) + d.q0 / 2;
+  const int2 c0 = __ldg(c), c1 = d.ntiles == 2 ? __ldg(c + 1) : make_int2(0, 0);
+  d.nkv_t[0] = min(max(c0.x, 1), g.topk);
+  d.nkv_t[1] = d.ntiles == 2 ? min(max(c1.x, 1), g.topk) : 0;
+  d.nsh_t[0] = c0.y;
+  d.nsh_t[1] = c1.y;
+  d.nkv = max(d.nkv_t[0], d.nkv_t[1]);
   return d;
 }
-// Selected key block j of query block qb (head h), checked against the block count.
-__device__ __forceinline__ int vsa_selected(const int32_t* __restrict__ sel, int h, int qb, int j,
-                                            const WindowAttnGeom& g, unsigned int* err) {
-  const int nblk = vsa_num_blocks(g);
-  const int b = __ldg(sel + (static_cast<size_t>(h) * nblk + qb) * g.topk + j);
-  if (b < 0 || b >= nblk) {
-    record_error(err, kErrBadBlockIndex);
-    return 0;
-  }
-  return b;
+// Step j of pair p (head h): the two key blocks of the step and which query block uses each.
+__device__ __forceinline__ uint2 vsa_step(const uint2* __restrict__ steps, int h, int p, int j,
+                                          const WindowAttnGeom& g) {
+  return __ldg(steps + (static_cast<size_t>(h) * ((vsa_num_blocks(g) + 1) / 2) + p) * g.topk + j);
 }
 
 __device__ __forceinline__ int checked_len(const int32_t* __restrict__ cu, int g, int capacity,
@@ -386,8 +389,9 @@ __device__ __forceinline__ void vsa_load_tile(uint8_t* dst, const CUtensorMap* m
 // kModeWindow: windows of a (T, H, W) grid read in place (5-D tensor maps over [T, H, W, heads, D]
 // in row-major token order); the output goes back to the same positions.
 // kModeVsa: 64-token blocks of the grid read in place; each 64-row half of a query tile is one
-// query block and attends to its own selected key blocks (vsa_sel), which fill the same half of
-// every key/value tile.  The two query tiles of an item have separate key/value streams.
+// query block.  Key/value tiles follow the pair's schedule (vsa_steps): each step stacks two key
+// blocks, and each query block attends to the halves the step marks as its own.  The two query
+// tiles of an item have separate key/value streams.
 template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -399,7 +403,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 float* __restrict__ lse, const int32_t* __restrict__ cu_seqlens, int num_segments,
                 int capacity, int num_heads, float scale, float scale_log2,
                 uint32_t* __restrict__ ws, const __grid_constant__ WindowAttnGeom wg,
-                const int32_t* __restrict__ vsa_sel, unsigned int* err) {
+                const uint2* __restrict__ vsa_steps, const int2* __restrict__ vsa_counts,
+                unsigned int* err) {
   constexpr bool kWin = kMode == kModeWindow;
   constexpr bool kVsa = kMode == kModeVsa;
   using C = Cfg<D, kMode>;
@@ -481,42 +486,38 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // VSA: stream an item's selected key (or value) blocks through one ring, per step the tile of
-  // query tile 0 then of tile 1 (the order the MMA warp consumes them); block ids are fetched one
-  // step ahead.  K and V have a producer thread each (warps 8 and 10), so a wait on one ring never
-  // holds back loads for the other.  Returns false when a wait ran out.
+  // VSA: stream an item's key (or value) tiles through one ring, per step the tile of query tile
+  // 0 then of tile 1 (the order the MMA warp consumes them; a tile whose schedule has ended is
+  // skipped); each step's blocks are fetched one step ahead.  K and V have a producer thread each
+  // (warps 8 and 10), so a wait on one ring never holds back loads for the other.  Returns false
+  // when a wait ran out.
   auto vsa_stream = [&](const WorkDesc& d, auto stages, uint8_t* ring, const CUtensorMap* map,
                         uint32_t full0, uint32_t empty0, uint32_t& cnt) -> bool {
     constexpr int S = decltype(stages)::value;
-    const bool has1 = d.ntiles == 2;
-    int qb[2][2], cur[2][2], nxt[2][2];
-    vsa_item_blocks(d, wg, qb);
+    const int nt = d.ntiles;
+    uint2 cur[2], nxt[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        cur[t][h] = (t == 1 && !has1) ? 0 : vsa_selected(vsa_sel, d.head, qb[t][h], 0, wg, err);
+      cur[t] = t < nt ? vsa_step(vsa_steps, d.head, d.q0 / 2 + t, 0, wg) : make_uint2(0u, 0u);
     for (int j = 0; j < d.nkv; ++j) {
 #pragma unroll
       for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          nxt[t][h] = (j + 1 >= d.nkv || (t == 1 && !has1))
-                          ? 0 : vsa_selected(vsa_sel, d.head, qb[t][h], j + 1, wg, err);
+        nxt[t] = (t < nt && j + 1 < d.nkv_t[t]) ? vsa_step(vsa_steps, d.head, d.q0 / 2 + t, j + 1, wg)
+                                                 : make_uint2(0u, 0u);
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        if (t == 1 && !has1) break;
+        if (t >= nt || j >= d.nkv_t[t]) continue;
         const uint32_t s = cnt % S;
         if (!mbar_wait(empty0 + 8 * s, ((cnt / S) & 1) ^ 1)) return false;
         mbar_arrive_expect_tx(full0 + 8 * s, C::kTileBytes);
-        vsa_load_tile<C::kBoxes, C::kBoxBytes>(ring + s * C::kTileBytes, map, d.head, cur[t][0],
-                                               cur[t][1], full0 + 8 * s, wg);
+        vsa_load_tile<C::kBoxes, C::kBoxBytes>(ring + s * C::kTileBytes, map, d.head,
+                                               static_cast<int>(cur[t].x & kVsaBlockMask),
+                                               static_cast<int>(cur[t].y & kVsaBlockMask),
+                                               full0 + 8 * s, wg);
         ++cnt;
       }
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) cur[t][h] = nxt[t][h];
+      for (int t = 0; t < 2; ++t) cur[t] = nxt[t];
     }
     return true;
   };
@@ -543,7 +544,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
             if constexpr (kWin)
               d = decode_window(item, wg, num_heads);
             else if constexpr (kVsa)
-              d = decode_vsa(item, wg, num_heads);
+              d = decode_vsa(item, wg, vsa_counts);
             else
               d = decode_item(item, ws, cu_seqlens, num_segments, num_heads);
           } else {
@@ -681,7 +682,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           // Each query tile has its own K/V stream: per step the rings hold K of tile 0, K of
           // tile 1, then V of tile 0, V of tile 1.  Order per step j: PV0_j, S0_{j+1}, PV1_j,
           // S1_{j+1}, as for shared tiles.
+          // Tile t runs d.nkv_t[t] steps (its pair's schedule); a tile whose steps have ended is
+          // skipped.  The item's last QK^T is step nkv - 1 of the last tile with nkv steps.
           const int nt = has1 ? 2 : 1;
+          const int tlast = (has1 && d.nkv_t[1] == nkv) ? 1 : 0;
           ok = wait_all(bar_qfull(0), qn[0]++ & 1);
           if (ok && has1) ok = wait_all(bar_qfull(1), qn[1]++ & 1);
           for (int t = 0; t < nt && ok; ++t) {
@@ -698,8 +702,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
             ++kc;
           }
           for (int j = 0; j < nkv && ok; ++j) {
-            const bool more = j + 1 < nkv;
             for (int t = 0; t < nt; ++t) {
+              const int nkv_t = t == 0 ? d.nkv_t[0] : d.nkv_t[1];
+              if (j >= nkv_t) continue;
+              const bool more = j + 1 < nkv_t;
               const int sv = static_cast<int>(vc % SV);
               ok = wait_all(bar_vfull(sv), (vc / SV) & 1);
               if (ok) ok = wait_all(bar_pfull(t), pn[t]++ & 1);
@@ -714,7 +720,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 if (more) {
                   issue_qk(t, kc % SK);
                   mma_commit(bar_kempty(kc % SK));
-                  if (j + 2 == nkv && t == nt - 1) mma_commit(bar_qempty);
+                  if (j + 2 == nkv && t == tlast) mma_commit(bar_qempty);
                 }
               }
               __syncwarp();
@@ -906,63 +912,83 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
       };
       // VSA: this thread's half of the tile (warps 0-1 of the warpgroup: rows 0-63) is query
-      // block vqb; its keys fill the same half of every key tile, so it reads 64 columns of S
+      // block vqb.  Each step stacks two key blocks (columns 0-63 and 64-127 of S); the step says
+      // which of them this query block attends to (one or both), and only those are read.
       const int vhalf = (warp >> 1) & 1;
       int vqb = 0;
       if constexpr (kVsa) vqb = min(d.q0 + 2 * t + vhalf, vsa_num_blocks(wg) - 1);
-      for (int j = 0; j < nkv; ++j) {
-        uint64_t vkm = ~0ull;  // VSA: rows of this step's key block that lie inside the grid
+      const int nsteps = kVsa ? (t == 0 ? d.nkv_t[0] : d.nkv_t[1]) : nkv;
+      const int nshared = kVsa ? (t == 0 ? d.nsh_t[0] : d.nsh_t[1]) : 0;
+      for (int j = 0; j < nsteps; ++j) {
+        uint32_t use0 = 1u, use1 = 1u;          // VSA: this query block's halves of the key tile
+        uint64_t vkm0 = ~0ull, vkm1 = ~0ull;    // VSA: their key rows inside the grid
         if constexpr (kVsa) {
-          if (vsa_partial) vkm = vsa_block_mask(vsa_selected(vsa_sel, d.head, vqb, j, wg, err), wg);
+          // the schedule's layout: nshared / 2 steps of two shared blocks, the odd shared block
+          // in half 0, then this query block's own blocks in its own half
+          if (j >= nshared / 2) {
+            const bool odd = (nshared & 1) && j == nshared / 2;
+            use0 = odd || vhalf == 0;
+            use1 = !odd && vhalf == 1;
+          }
+          if (vsa_partial) {
+            const uint2 e = vsa_step(vsa_steps, d.head, d.q0 / 2 + t, j, wg);
+            vkm0 = vsa_block_mask(static_cast<int>(e.x & kVsaBlockMask), wg);
+            vkm1 = vsa_block_mask(static_cast<int>(e.y & kVsaBlockMask), wg);
+          }
         }
         ok = mbar_wait(bar_sfull(t), sn++ & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         if constexpr (kVsa) {
-          uint32_t sr[64];
-          tmem_ld32(s_addr + 64 * vhalf, sr);
-          tmem_ld32(s_addr + 64 * vhalf + 32, sr + 32);
-          tmem_ld_wait();
-          tmem_reg_fence<64>(sr);
-          float s[64];
+          if (!(use0 && use1)) {
+            // one key block of the step is this query block's: 64 columns of S
+            const int sl = use0 ? 0 : 1;
+            const uint64_t vkm = sl ? vkm1 : vkm0;
+            uint32_t sr[64];
+            tmem_ld32(s_addr + 64 * sl, sr);
+            tmem_ld32(s_addr + 64 * sl + 32, sr + 32);
+            tmem_ld_wait();
+            tmem_reg_fence<64>(sr);
+            float s[64];
 #pragma unroll
-          for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c]);
-          if (vkm != ~0ull) {
-            // key rows of an edge block outside the grid (zero-filled by TMA): -inf by select
+            for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c]);
+            if (vkm != ~0ull) {
+              // key rows of an edge block outside the grid (zero-filled by TMA): -inf by select
 #pragma unroll
-            for (int c = 0; c < 64; ++c) s[c] = ((vkm >> c) & 1ull) ? s[c] : -INFINITY;
+              for (int c = 0; c < 64; ++c) s[c] = ((vkm >> c) & 1ull) ? s[c] : -INFINITY;
+            }
+            // row max over the 64 columns: four chains, 3-input steps over 4..59, then 60..63
+            float m4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+            for (int c = 4; c < 60; c += 8)
+#pragma unroll
+              for (int u = 0; u < 4; ++u) m4[u] = fmax3(m4[u], s[c + u], s[c + 4 + u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) m4[u] = fmaxf(m4[u], s[60 + u]);
+            update_max(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), j);
+            const float mb = m_used * scale_log2;
+            const float2 nm2 = make_float2(-mb, -mb);
+            float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+            uint32_t p[32], z[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), c2, nm2);
+              const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              acc[c & 3] = fadd2(acc[c & 3], e);
+              p[c] = pack_bf16x2(e.x, e.y);
+              z[c] = 0u;
+            }
+            const float2 a01 = fadd2(acc[0], acc[1]);
+            const float2 a23 = fadd2(acc[2], acc[3]);
+            l += (a01.x + a01.y) + (a23.x + a23.y);
+            // P over S: this block's keys get P, the other block's keys weight 0 for these rows
+            tmem_st32(s_addr + 32 * sl, p);
+            tmem_st32(s_addr + 32 * (1 - sl), z);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar_pfull(t));
+            continue;
           }
-          // row max over the 64 columns: four chains, 3-input steps over 4..59, then 60..63
-          float m4[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-          for (int c = 4; c < 60; c += 8)
-#pragma unroll
-            for (int u = 0; u < 4; ++u) m4[u] = fmax3(m4[u], s[c + u], s[c + 4 + u]);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) m4[u] = fmaxf(m4[u], s[60 + u]);
-          update_max(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), j);
-          const float mb = m_used * scale_log2;
-          const float2 nm2 = make_float2(-mb, -mb);
-          float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-          uint32_t p[32], z[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), c2, nm2);
-            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            acc[c & 3] = fadd2(acc[c & 3], e);
-            p[c] = pack_bf16x2(e.x, e.y);
-            z[c] = 0u;
-          }
-          const float2 a01 = fadd2(acc[0], acc[1]);
-          const float2 a23 = fadd2(acc[2], acc[3]);
-          l += (a01.x + a01.y) + (a23.x + a23.y);
-          // P over S: this half's keys get P, the other block's keys weight 0 for these rows
-          tmem_st32(s_addr + 32 * vhalf, p);
-          tmem_st32(s_addr + 32 * (1 - vhalf), z);
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(bar_pfull(t));
-          continue;
         }
         uint32_t sr[128];
         tmem_ld32(s_addr + 0, sr + 0);
@@ -982,6 +1008,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           if ((km[0] & km[1] & km[2] & km[3]) != 0xffffffffu) {
 #pragma unroll
             for (int c = 0; c < 128; ++c) s[c] = ((km[c >> 5] >> (c & 31)) & 1u) ? s[c] : -INFINITY;
+          }
+        } else if constexpr (kVsa) {
+          // key rows of edge blocks outside the grid (zero-filled by TMA): -inf by select
+          if ((vkm0 & vkm1) != ~0ull) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              s[c] = (((c < 64 ? vkm0 : vkm1) >> (c & 63)) & 1ull) ? s[c] : -INFINITY;
           }
         } else if (j == nkv - 1 && kv_last_valid < kBlockN) {
           // keys past the segment end: -inf by select, so a NaN/Inf score there is discarded
@@ -1010,10 +1043,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           acc[c & 3] = fadd2(acc[c & 3], e);
           p[c] = pack_bf16x2(e.x, e.y);
         }
-        tmem_st32(s_addr + 0, p + 0);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar_phalf(t));
+        if constexpr (!kVsa) {
+          tmem_st32(s_addr + 0, p + 0);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar_phalf(t));
+        }
 #pragma unroll
         for (int c = 32; c < 64; ++c) {
           const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), c2, nm2);
@@ -1024,6 +1059,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const float2 a01 = fadd2(acc[0], acc[1]);
         const float2 a23 = fadd2(acc[2], acc[3]);
         l += (a01.x + a01.y) + (a23.x + a23.y);
+        if constexpr (kVsa) tmem_st32(s_addr + 0, p + 0);  // VSA issues PV in one piece
         tmem_st32(s_addr + 32, p + 32);
         tmem_st_wait();
         tc_fence_before();
@@ -1156,7 +1192,8 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
   attn_fwd_kernel<D, kMode><<<grid, kThreads, C::kSmemBytes, stream>>>(
       a.tmap_q, a.tmap_k, a.tmap_v, half ? a.tmap_q2 : a.tmap_q, half ? a.tmap_k2 : a.tmap_k,
       half ? a.tmap_v2 : a.tmap_v, static_cast<__nv_bfloat16*>(a.o), a.lse, a.cu_seqlens,
-      a.num_segments, a.capacity, a.num_heads, a.scale, scale_log2, ws, a.wg, a.vsa_sel, a.err);
+      a.num_segments, a.capacity, a.num_heads, a.scale, scale_log2, ws, a.wg, a.vsa_steps,
+      a.vsa_counts, a.err);
   return cudaGetLastError();
 }
 

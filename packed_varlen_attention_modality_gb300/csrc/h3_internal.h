@@ -76,7 +76,9 @@ struct AttnArgs {
   CUtensorMap tmap_q2, tmap_k2, tmap_v2;
   int mode;            // kAttnModePacked / kAttnModeWindow / kAttnModeVsa
   WindowAttnGeom wg;
-  const int32_t* vsa_sel;  // VSA: [num_heads, nblk, topk] selected key blocks
+  // VSA: the key/value steps of every (head, pair of query blocks), from launch_vsa_schedule
+  const uint2* vsa_steps;
+  const int2* vsa_counts;
   void* o;
   float* lse;
   const int32_t* cu_seqlens;
@@ -105,6 +107,22 @@ size_t vsa_pool_bytes(int nblk, int heads, int head_dim);
 cudaError_t launch_vsa_select(const void* q, const void* k, const VsaGeom& g, int heads,
                               int head_dim, int topk, float scale, float* scores, int32_t* sel,
                               void* workspace, cudaStream_t stream);
+
+// VSA key/value schedule.  Query blocks 2p and 2p + 1 (the two halves of one 128-row tile; the
+// second is block 2p again past the last block) form pair p.  Step j of pair p loads two key
+// blocks into the two 64-row halves of a key tile: steps[(h * npairs + p) * topk + j] holds
+// {block of half 0 | use0 << kVsaUseShift, block of half 1 | use1 << kVsaUseShift}, where bit q
+// of use_s says whether query block 2p + q attends to that half's keys.  counts[h * npairs + p]
+// = {steps used (<= topk), s = blocks both query blocks selected}.  The steps follow a fixed
+// layout: s / 2 steps of two shared blocks (both halves used by both), one step with the odd
+// shared block in half 0 when s is odd, then steps whose half q is query block 2p + q's own.
+constexpr int kVsaUseShift = 28;
+constexpr uint32_t kVsaBlockMask = (1u << kVsaUseShift) - 1u;
+inline int vsa_pairs(int nblk) { return (nblk + 1) / 2; }
+size_t vsa_schedule_bytes(int nblk, int heads, int topk);
+// sel: int32 [heads, nblk, topk]; workspace: vsa_schedule_bytes() bytes, 16-byte aligned.
+cudaError_t launch_vsa_schedule(const int32_t* sel, int nblk, int heads, int topk, void* workspace,
+                                unsigned int* err, cudaStream_t stream);
 
 // ---- continuation window ---------------------------------------------------------------------
 struct ContinuationGeom {

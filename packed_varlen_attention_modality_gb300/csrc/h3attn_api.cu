@@ -559,10 +559,22 @@ h3_status h3_vsa_select(const void* q, const void* k, const int32_t grid[3],
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t h3_vsa_attn_workspace_size(const int32_t grid[3], const int32_t block[3],
+                                  int32_t num_heads, int32_t topk) {
+  h3::VsaGeom g;
+  if (grid == nullptr || block == nullptr ||
+      vsa_geometry(grid, block, num_heads, 128, &g) != H3_OK)
+    return 0;
+  const int nblk = g.nb[0] * g.nb[1] * g.nb[2];
+  if (topk < 1 || topk > nblk) return 0;
+  return h3::vsa_schedule_bytes(nblk, num_heads, topk);
+}
+
 h3_status h3_vsa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                           const int32_t grid[3], const int32_t block[3], int32_t num_heads,
                           int32_t head_dim, const int32_t* block_idx, int32_t topk,
-                          float softmax_scale, h3_stream_t stream) {
+                          float softmax_scale, void* workspace, size_t workspace_bytes,
+                          h3_stream_t stream) {
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || grid == nullptr ||
       block == nullptr || block_idx == nullptr)
     return H3_ERR_NULL;
@@ -570,13 +582,18 @@ h3_status h3_vsa_attn_fwd(const void* q, const void* k, const void* v, void* o, 
   const h3_status st = vsa_geometry(grid, block, num_heads, head_dim, &g);
   if (st != H3_OK) return st;
   const int64_t nblk = static_cast<int64_t>(g.nb[0]) * g.nb[1] * g.nb[2];
-  if (topk < 1 || topk > nblk) return H3_ERR_INVALID_ARG;
+  if (topk < 1 || topk > nblk || nblk > static_cast<int64_t>(h3::kVsaBlockMask))
+    return H3_ERR_INVALID_ARG;
   if (!(softmax_scale <= 0.f || std::isfinite(softmax_scale))) return H3_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+  const size_t need = h3::vsa_schedule_bytes(static_cast<int>(nblk), num_heads, topk);
+  if (workspace == nullptr || workspace_bytes < need) return H3_ERR_WORKSPACE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(workspace) ||
       (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
       (reinterpret_cast<uintptr_t>(block_idx) & 3u))
     return H3_ERR_MISALIGNED;
   if (!device_is_sm103()) return H3_ERR_UNSUPPORTED;
+  unsigned int* err = device_error_ptr();
+  if (err == nullptr) return H3_ERR_CUDA;
 
   h3::AttnArgs a{};
   a.mode = h3::kAttnModeVsa;
@@ -587,7 +604,10 @@ h3_status h3_vsa_attn_fwd(const void* q, const void* k, const void* v, void* o, 
     a.wg.nwin[ax] = g.nb[ax];
   }
   a.wg.topk = topk;
-  a.vsa_sel = block_idx;
+  const size_t pairs = static_cast<size_t>(num_heads) * h3::vsa_pairs(static_cast<int>(nblk));
+  a.vsa_steps = static_cast<const uint2*>(workspace);
+  a.vsa_counts = reinterpret_cast<const int2*>(static_cast<const uint8_t*>(workspace) +
+                                              (pairs * topk * 8 + 255) / 256 * 256);
   // one block (bw x bh x bt = 64 rows) per box
   if (!make_window_map(&a.tmap_q, q, grid, block, block[0], num_heads, head_dim) ||
       !make_window_map(&a.tmap_k, k, grid, block, block[0], num_heads, head_dim) ||
@@ -599,9 +619,13 @@ h3_status h3_vsa_attn_fwd(const void* q, const void* k, const void* v, void* o, 
   a.num_heads = num_heads;
   a.head_dim = head_dim;
   a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(head_dim));
-  a.err = device_error_ptr();
-  if (a.err == nullptr) return H3_ERR_CUDA;
-  return from_cuda(h3::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
+  a.err = err;
+  // the pairs' key/value schedule, then the attention that follows it (same stream)
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t ce = h3::launch_vsa_schedule(block_idx, static_cast<int>(nblk), num_heads,
+                                                 topk, workspace, err, cs);
+  if (ce != cudaSuccess) return from_cuda(ce);
+  return from_cuda(h3::launch_attn_fwd(a, cs));
 }
 
 int32_t h3_window_count(const int32_t grid[3], const int32_t win[3], const int32_t shift[3]) {

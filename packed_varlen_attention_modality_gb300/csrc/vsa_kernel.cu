@@ -16,11 +16,22 @@
 //   vsa_topk_kernel    one warp per (head, query block): 8-bit radix select of the k-th largest
 //                      score over 4 passes (the row stays in L1/L2), then an ascending ballot
 //                      compaction that takes the ties at the threshold lowest id first
+//
+// And the attention's key/value schedule (vsa_schedule_kernel, one warp per head and pair of
+// query blocks).  The token-level attention runs a 128-row query tile as two query blocks, one
+// per 64-row half, and each step loads a 128-row key tile as two key blocks.  A block that both
+// query blocks selected serves both halves, so two such blocks fill a step with no masked work;
+// a block only one of them selected is paired with one only the other selected, as before.  With
+// s shared selections a pair takes ceil(s / 2) + (topk - s) steps instead of topk.  Sorted lists
+// (as vsa_topk_kernel writes them) are intersected as multisets by binary search; lists in any
+// other order, or with an id out of range (recorded, then read as block 0), keep one step per
+// list entry.
 #include <cuda_bf16.h>
 
 #include <cstdint>
 
 #include "h3_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace h3 {
 namespace {
@@ -30,6 +41,7 @@ constexpr int kScoreRows = 64;     // query blocks per score tile
 constexpr int kScoreCols = 256;    // key blocks per score tile
 constexpr int kScoreThreads = 256;
 constexpr int kTopkWarps = 8;
+constexpr int kSchedWarps = 8;
 
 // Block b of the grid: origin and extent (cropped by the grid edge).
 struct BlockBox {
@@ -226,6 +238,106 @@ vsa_topk_kernel(const float* __restrict__ scores, int rows, int nblk, int topk,
   }
 }
 
+// First index in a[0, n) whose value is >= x (a ascending).
+__device__ __forceinline__ int lower_idx(const int32_t* __restrict__ a, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(a + mid) < x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+// Entries equal to x in a[0, n) (a ascending).
+__device__ __forceinline__ int count_of(const int32_t* __restrict__ a, int n, int x) {
+  const int lo = lower_idx(a, n, x);
+  int hi = n, l = lo;
+  while (l < hi) {
+    const int mid = (l + hi) >> 1;
+    if (__ldg(a + mid) <= x) l = mid + 1; else hi = mid;
+  }
+  return l - lo;
+}
+
+__global__ void __launch_bounds__(kSchedWarps * 32)
+vsa_schedule_kernel(const int32_t* __restrict__ sel, int nblk, int heads, int topk,
+                    uint32_t* __restrict__ steps, int2* __restrict__ counts, unsigned int* err) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int npairs = (nblk + 1) / 2;
+  const int pid = blockIdx.x * kSchedWarps + warp;  // h * npairs + p
+  if (pid >= heads * npairs) return;
+  const int h = pid / npairs, p = pid % npairs;
+  const int32_t* A = sel + (static_cast<size_t>(h) * nblk + 2 * p) * topk;
+  const int32_t* B = sel + (static_cast<size_t>(h) * nblk + min(2 * p + 1, nblk - 1)) * topk;
+  uint32_t* out = steps + static_cast<size_t>(pid) * topk * 2;  // [topk][half]
+  const unsigned lt = (1u << lane) - 1u;
+  bool valid = true, sorted = true;
+  for (int i = lane; i < topk; i += 32) {
+    const int a = __ldg(A + i), b = __ldg(B + i);
+    valid = valid && a >= 0 && a < nblk && b >= 0 && b < nblk;
+    if (i > 0) sorted = sorted && __ldg(A + i - 1) <= a && __ldg(B + i - 1) <= b;
+  }
+  valid = __all_sync(0xffffffffu, valid);
+  sorted = __all_sync(0xffffffffu, sorted);
+  if (!valid && lane == 0) record_error(err, kErrBadBlockIndex);
+  if (!valid || !sorted) {
+    for (int j = lane; j < topk; j += 32) {
+      int a = __ldg(A + j), b = __ldg(B + j);
+      if (a < 0 || a >= nblk) a = 0;
+      if (b < 0 || b >= nblk) b = 0;
+      out[2 * j] = static_cast<uint32_t>(a) | (1u << kVsaUseShift);
+      out[2 * j + 1] = static_cast<uint32_t>(b) | (2u << kVsaUseShift);
+    }
+    if (lane == 0) counts[pid] = make_int2(topk, 0);
+    return;
+  }
+  // entry i of A is shared when fewer copies of its id precede it in A than B holds (and the
+  // other way round for B): the multiset intersection, taken in list order
+  auto shared_a = [&](int i) {
+    const int x = __ldg(A + i);
+    return i - lower_idx(A, i, x) < count_of(B, topk, x);
+  };
+  auto shared_b = [&](int j) {
+    const int y = __ldg(B + j);
+    return j - lower_idx(B, j, y) < count_of(A, topk, y);
+  };
+  int ns = 0;
+  for (int i0 = 0; i0 < topk; i0 += 32) {
+    const int i = i0 + lane;
+    ns += __popc(__ballot_sync(0xffffffffu, i < topk && shared_a(i)));
+  }
+  const int s0 = (ns + 1) / 2;  // steps of shared blocks
+  // shared blocks two per step, both halves; then A's own blocks in half 0 beside B's own in half 1
+  int nc = 0, na = 0;
+  for (int i0 = 0; i0 < topk; i0 += 32) {
+    const int i = i0 + lane;
+    const bool in = i < topk;
+    const bool c = in && shared_a(i);
+    const unsigned cm = __ballot_sync(0xffffffffu, c), am = __ballot_sync(0xffffffffu, in && !c);
+    if (in) {
+      const uint32_t x = static_cast<uint32_t>(__ldg(A + i));
+      if (c) {
+        const int r = nc + __popc(cm & lt);
+        out[2 * (r >> 1) + (r & 1)] = x | (3u << kVsaUseShift);
+        if (r == ns - 1 && (ns & 1)) out[2 * (r >> 1) + 1] = x;  // odd one out: other half unused
+      } else {
+        out[2 * (s0 + na + __popc(am & lt))] = x | (1u << kVsaUseShift);
+      }
+    }
+    nc += __popc(cm);
+    na += __popc(am);
+  }
+  int nb = 0;
+  for (int j0 = 0; j0 < topk; j0 += 32) {
+    const int j = j0 + lane;
+    const bool own = j < topk && !shared_b(j);
+    const unsigned bm = __ballot_sync(0xffffffffu, own);
+    if (own)
+      out[2 * (s0 + nb + __popc(bm & lt)) + 1] = static_cast<uint32_t>(__ldg(B + j)) | (2u << kVsaUseShift);
+    nb += __popc(bm);
+  }
+  if (lane == 0) counts[pid] = make_int2(s0 + (topk - ns), ns);
+}
+
 template <int D>
 cudaError_t launch_score(dim3 grid, const float* qm, const float* km, int nblk, float scale,
                          float* scores, cudaStream_t stream) {
@@ -246,6 +358,23 @@ cudaError_t launch_score(dim3 grid, const float* qm, const float* km, int nblk, 
 }
 
 }  // namespace
+
+size_t vsa_schedule_bytes(int nblk, int heads, int topk) {
+  const size_t pairs = static_cast<size_t>(heads) * vsa_pairs(nblk);
+  return (pairs * topk * 8 + 255) / 256 * 256 + (pairs * 8 + 255) / 256 * 256;
+}
+
+cudaError_t launch_vsa_schedule(const int32_t* sel, int nblk, int heads, int topk, void* workspace,
+                                unsigned int* err, cudaStream_t stream) {
+  const size_t pairs = static_cast<size_t>(heads) * vsa_pairs(nblk);
+  uint32_t* steps = static_cast<uint32_t*>(workspace);
+  int2* counts = reinterpret_cast<int2*>(static_cast<uint8_t*>(workspace) +
+                                         (pairs * topk * 8 + 255) / 256 * 256);
+  const unsigned blocks = static_cast<unsigned>((pairs + kSchedWarps - 1) / kSchedWarps);
+  vsa_schedule_kernel<<<blocks, kSchedWarps * 32, 0, stream>>>(sel, nblk, heads, topk, steps,
+                                                               counts, err);
+  return cudaGetLastError();
+}
 
 size_t vsa_pool_bytes(int nblk, int heads, int head_dim) {
   const size_t b = 2ull * heads * nblk * head_dim * sizeof(float);

@@ -186,14 +186,26 @@ def test_vsa_calls_reject_bad_arguments_on_the_host(lib):
     assert sel(w=0) == 5 and sel(wsb=ws - 1) == 5
     assert sel(q=FAKE + 8) == 8 and sel(scores=FAKE + 2) == 8
 
-    def attn(q=FAKE, topk=3, D=128, block=b, idx=FAKE):
+    aws = lib.h3_vsa_attn_workspace_size(g, b, 2, 3)
+    assert aws > 0 and lib.h3_vsa_attn_workspace_size(g, b, 2, 9) == 0
+
+    def attn(q=FAKE, topk=3, D=128, block=b, idx=FAKE, w=FAKE, wsb=aws):
         return lib.h3_vsa_attn_fwd(P(q) if q else None, P(FAKE), P(FAKE), P(FAKE), None, g, block, 2, D,
-                                   P(idx) if idx else None, topk, 0.0, None)
+                                   P(idx) if idx else None, topk, 0.0, P(w) if w else None, wsb, None)
 
     assert attn(q=0) == 1 and attn(idx=0) == 1
     assert attn(topk=0) == 2 and attn(topk=9) == 2
     assert attn(D=64, block=_i3((2, 2, 2))) == 4
-    assert attn(q=FAKE + 8) == 8 and attn(idx=FAKE + 2) == 8
+    assert attn(w=0) == 5 and attn(wsb=aws - 1) == 5
+    assert attn(q=FAKE + 8) == 8 and attn(idx=FAKE + 2) == 8 and attn(w=FAKE + 8) == 8
+
+
+def test_vsa_attn_workspace_holds_the_schedule(lib):
+    # 2016 blocks -> 1008 pairs per head; 8 bytes per step, topk steps per pair, plus a count per pair
+    ws = lib.h3_vsa_attn_workspace_size(_i3((32, 48, 84)), _i3((4, 4, 4)), 24, 252)
+    assert ws >= 24 * 1008 * (252 * 8 + 4)
+    assert lib.h3_vsa_attn_workspace_size(_i3((32, 48, 84)), _i3((4, 4, 4)), 24, 2017) == 0
+    assert lib.h3_vsa_attn_workspace_size(_i3((32, 48, 84)), _i3((4, 4, 8)), 24, 1) == 0
 
 
 def _plan_fields(p):

@@ -238,3 +238,89 @@ def test_non_cubic_64_token_blocks(h3, dev, block):
     ref_o, ref_lse = oracle.vsa_attention(q, k, v, grid, block, sel_np)
     _close(o.float().cpu().numpy(), ref_o, f"vsa block {block}")
     _lse_close(lse.cpu().numpy(), ref_lse, f"vsa block {block}")
+
+
+def _schedule(ws, H, nblk, topk):
+    """The key/value schedule in the attention's workspace: per (head, pair) the step list
+    [topk, 2] of (block | use << 28) words, the step count and the shared-block count."""
+    pairs = H * ((nblk + 1) // 2)
+    raw = ws.cpu().numpy()
+    off = (pairs * topk * 8 + 255) // 256 * 256
+    steps = raw[:pairs * topk * 8].view(np.uint32).reshape(H, -1, topk, 2)
+    counts = raw[off:off + pairs * 8].view(np.int32).reshape(H, -1, 2)
+    return steps, counts[..., 0], counts[..., 1]
+
+
+def _overlap_lists(case, nblk, topk, rng):
+    """Selection lists [nblk, topk] whose paired query blocks (2p, 2p + 1) share a chosen number
+    of blocks."""
+    sel = np.zeros((nblk, topk), np.int32)
+    for p in range(0, nblk, 2):
+        a = np.sort(rng.choice(nblk, topk, replace=False))
+        if case == "identical":
+            b = a.copy()
+        elif case == "disjoint":
+            rest = np.setdiff1d(np.arange(nblk), a)
+            b = np.sort(rng.choice(rest, topk, replace=False))
+        elif case == "odd_overlap":       # 3 shared, the rest disjoint
+            rest = np.setdiff1d(np.arange(nblk), a)
+            b = np.sort(np.concatenate([a[:3], rng.choice(rest, topk - 3, replace=False)]))
+        elif case == "repeats":           # sorted lists with repeated ids (each copy counts)
+            a = np.sort(rng.choice(4, topk))
+            b = np.sort(rng.choice(4, topk))
+        elif case == "one_unsorted":      # pair 0's second list reversed: one step per entry there
+            b = np.sort(rng.choice(nblk, topk, replace=False))
+            if p == 0:
+                b = b[::-1].copy()
+        else:                             # random sorted lists
+            b = np.sort(rng.choice(nblk, topk, replace=False))
+        sel[p] = a
+        if p + 1 < nblk:
+            sel[p + 1] = b
+    return sel
+
+
+SCHEDULE_CASES = ["identical", "disjoint", "odd_overlap", "repeats", "one_unsorted", "random"]
+
+
+@pytest.mark.parametrize("case", SCHEDULE_CASES)
+@pytest.mark.parametrize("D", [64, 128])
+def test_shared_blocks_schedule_against_oracle(h3, dev, case, D):
+    """Paired query blocks that select the same key blocks share steps: the schedule in the
+    workspace takes ceil(s/2) + topk - s steps for s shared selections of sorted lists (topk for
+    unsorted ones), marks for each query block exactly its own list (as a multiset), and the
+    attention over it equals the oracle's.  Grid 5x9x11: 18 blocks, ragged on every axis."""
+    grid, H, topk = (5, 9, 11), 2, 6
+    n = grid[0] * grid[1] * grid[2]
+    nblk = oracle.vsa_block_count(grid, (4, 4, 4))
+    rng = np.random.default_rng(100 * SCHEDULE_CASES.index(case) + D)
+    sel = np.stack([_overlap_lists(case, nblk, topk, rng) for _ in range(H)])
+    q, k, v = _qkv(21 + D, n, H, D)
+    ws = torch.empty(h3.vsa_attn_workspace_size(grid, (4, 4, 4), H, topk), dtype=torch.uint8, device=dev)
+    o, lse = h3.vsa_attn_fwd(q.to(dev), k.to(dev), v.to(dev), grid, torch.from_numpy(sel).to(dev),
+                             return_lse=True, workspace=ws)
+    torch.cuda.synchronize()
+    assert h3.get_device_error(dev) == 0
+    steps, nsteps, nshared = _schedule(ws, H, nblk, topk)
+    for h in range(H):
+        for p in range((nblk + 1) // 2):
+            a, b = sel[h, 2 * p], sel[h, min(2 * p + 1, nblk - 1)]
+            sorted_ = np.all(np.diff(a) >= 0) and np.all(np.diff(b) >= 0)
+            shared = sum(min(np.count_nonzero(a == x), np.count_nonzero(b == x)) for x in np.unique(a))
+            want = (shared + 1) // 2 + topk - shared if sorted_ else topk
+            assert nsteps[h, p] == want, (case, h, p, nsteps[h, p], want)
+            assert nshared[h, p] == (shared if sorted_ else 0)
+            st = steps[h, p, :want]
+            blk, use = st & ((1 << 28) - 1), st >> 28
+            # the fixed layout the attention relies on: shared pairs, the odd shared block in
+            # half 0, then each query block's own blocks in its own half
+            s2 = nshared[h, p]
+            lay = np.array([[3, 3]] * (s2 // 2) + [[3, 0]] * (s2 & 1) + [[1, 2]] * (want - (s2 + 1) // 2))
+            assert np.array_equal(use, lay), (case, h, p)
+            for qb, lst in ((0, a), (1, b)):
+                mine = np.sort(blk[(use >> qb) & 1 == 1])
+                assert np.array_equal(mine, np.sort(lst)), (case, h, p, qb)
+            assert np.all(blk < nblk)
+    ref_o, ref_lse = oracle.vsa_attention(q, k, v, grid, (4, 4, 4), sel)
+    _close(o.float().cpu().numpy(), ref_o, f"schedule {case} D {D}")
+    _lse_close(lse.cpu().numpy(), ref_lse, f"schedule {case} D {D}")

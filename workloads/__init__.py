@@ -290,6 +290,24 @@ def vsa_video(seed: int = 7, grid=(32, 48, 84), block=(4, 4, 4), heads: int = 24
                        topk=k_sel, q=q, k=k, v=v)
 
 
+def vsa_paired_selection(seed: int, heads: int, nblk: int, topk: int, shared: int) -> np.ndarray:
+    """A block selection int32 [heads, nblk, topk] (ascending ids, distinct per list) in which
+    query blocks 2p and 2p + 1 have exactly `shared` selected blocks in common and the rest drawn
+    at random from the other blocks: a stand-in for the overlap of neighbouring query blocks'
+    selections on spatially coherent latents (random N(0,1) inputs give about topk^2 / nblk)."""
+    rng = np.random.default_rng(seed)
+    sel = np.empty((heads, nblk, topk), np.int32)
+    for h in range(heads):
+        for p in range(0, nblk, 2):
+            a = rng.choice(nblk, topk, replace=False)
+            rest = np.setdiff1d(np.arange(nblk), a)
+            b = np.concatenate([a[:shared], rng.choice(rest, topk - shared, replace=False)])
+            sel[h, p] = np.sort(a)
+            if p + 1 < nblk:
+                sel[h, p + 1] = np.sort(b)
+    return sel
+
+
 WORKLOADS = {
     "tiny_example": tiny_example,
     "single_request_4k": single_request_4k,
