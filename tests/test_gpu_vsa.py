@@ -324,3 +324,27 @@ def test_shared_blocks_schedule_against_oracle(h3, dev, case, D):
     ref_o, ref_lse = oracle.vsa_attention(q, k, v, grid, (4, 4, 4), sel)
     _close(o.float().cpu().numpy(), ref_o, f"schedule {case} D {D}")
     _lse_close(lse.cpu().numpy(), ref_lse, f"schedule {case} D {D}")
+
+
+def test_shared_half_selection_at_bench_size_sampled(h3, dev):
+    """The bench's fixed selection on the 1344x768 latent: paired query blocks share 126 of their
+    252 blocks, so half of each pair's steps serve both halves of the tile.  Sampled query blocks
+    of three heads against the oracle."""
+    wl = W.vsa_video()
+    grid, block, topk = wl.grid, wl.block, wl.topk
+    nblk = oracle.vsa_block_count(grid, block)
+    sel_np = W.vsa_paired_selection(9, wl.num_heads, nblk, topk, topk // 2)
+    o, lse = h3.vsa_attn_fwd(wl.q.to(dev), wl.k.to(dev), wl.v.to(dev), grid,
+                             torch.from_numpy(sel_np).to(dev), return_lse=True)
+    torch.cuda.synchronize()
+    assert h3.get_device_error(dev) == 0
+    rng = np.random.default_rng(16)
+    blocks = np.unique(np.concatenate([[0, 1, 2, 3, nblk - 2, nblk - 1], rng.choice(nblk, 10, replace=False)]))
+    heads = [0, 11, 23]
+    ids = oracle.vsa_block_ids(grid, block)
+    rows = np.nonzero(np.isin(ids, blocks))[0]
+    ref_o, ref_lse = oracle.vsa_attention(wl.q[:, heads], wl.k[:, heads], wl.v[:, heads], grid, block,
+                                          sel_np[heads], rows=rows)
+    got = o.float().cpu().numpy()[:, heads]
+    _close(got[rows], ref_o[rows], "vsa 32x48x84 shared-half sampled")
+    _lse_close(lse.cpu().numpy()[heads][:, rows], ref_lse[:, rows], "vsa 32x48x84 shared-half sampled")
