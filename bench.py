@@ -187,8 +187,106 @@ def cpu_baseline(wl, n_rows=512):
                       f"{len(os.sched_getaffinity(0))} cores"}
 
 
+def _cpu_threads(ru0, ru1, wall):
+    cpu = (ru1.ru_utime - ru0.ru_utime) + (ru1.ru_stime - ru0.ru_stime)
+    return max(1, round(cpu / wall)) if wall > 0 else 1
+
+
+def _reference_line(args, metric, value, unit, higher, ms, config, threads, sample):
+    return {"metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": higher, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference", "config": config,
+            "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def _reference_full_packed(args):
+    """The oracle's whole pass (fp64 RoPE of Q and K, then attention over every row) each step:
+    the worked example and the 4,096-token request are small enough to time in full."""
+    import oracle
+    import workloads
+
+    wl = workloads.WORKLOADS[args.workload]()
+    times, threads = [], 1
+    for i in range(args.warmup + args.steps):
+        ru0, t0 = resource.getrusage(resource.RUSAGE_SELF), time.perf_counter()
+        qr = oracle.rope_apply(wl.q, wl.pos, wl.tag, wl.cu_requests, wl.start_frames)
+        kr = oracle.rope_apply(wl.k, wl.pos, wl.tag, wl.cu_requests, wl.start_frames)
+        oracle.varlen_attention(qr, kr, wl.v, wl.cu_seqlens)
+        t1, ru1 = time.perf_counter(), resource.getrusage(resource.RUSAGE_SELF)
+        if i >= args.warmup:
+            times.append(t1 - t0)
+            threads = _cpu_threads(ru0, ru1, t1 - t0)
+    sec = float(np.mean(times))
+    config = {"workload": wl.name, "tokens": wl.num_tokens, "heads": wl.num_heads, "head_dim": wl.head_dim,
+              "cu_seqlens": [int(x) for x in wl.cu_seqlens]}
+    sample = "the whole pass each step: fp64 RoPE of Q and K, then fp64 attention over every row"
+    if args.workload == "tiny_example":
+        line = _reference_line(args, "worked-example step latency (RoPE + varlen attention, 45 tokens)",
+                               sec * 1e6, "us", False, sec * 1e3, config, threads, sample)
+    else:
+        line = _reference_line(args, f"packed varlen attn TFLOP/s ({wl.name})",
+                               wl.attention_flops() / sec / 1e12, UNIT, True, sec * 1e3, config, threads,
+                               sample)
+    print(json.dumps(line), flush=True)
+
+
+def _reference_window(args, windows_per_layer=4):
+    """Both window layers of the 32x48x84 grid on a sample: each step draws windows of each layer
+    uniformly at random, packs their rows, runs fp64 attention and restores them; each layer's
+    time is scaled to the whole layer by its window count (an unbiased estimate of the whole
+    layer's time; one full layer takes minutes here)."""
+    import oracle
+    from workloads import window_grid
+
+    wl = window_grid()
+    H, D = wl.num_heads, wl.head_dim
+    shifts = [wl.shift if sh else (0, 0, 0) for sh in wl.layer_shifted]
+    total_flops = 0.0
+    parts = []
+    for sh in shifts:
+        perm, cu = oracle.window_partition(wl.grid, wl.window, sh)
+        sizes = np.diff(cu).astype(np.float64)
+        parts.append((perm, cu, sizes))
+        total_flops += 4.0 * H * D * float(np.sum(sizes ** 2))
+    out = np.zeros((wl.num_tokens, H, D))  # the layer's output in grid order (allocated once)
+    times, threads = [], 1
+    for i in range(args.warmup + args.steps):
+        rng = np.random.default_rng(500 + i)
+        job = 0.0
+        for (perm, cu, sizes), (q, k, v) in zip(parts, wl.layers):
+            pick = np.sort(rng.choice(sizes.size, windows_per_layer, replace=False))
+            ru0, t0 = resource.getrusage(resource.RUSAGE_SELF), time.perf_counter()
+            rows = np.concatenate([perm[cu[w]:cu[w + 1]] for w in pick])
+            sub_cu = np.concatenate([[0], np.cumsum(sizes[pick])]).astype(np.int64)
+            qp, kp, vp = (oracle.window_pack(x, rows) for x in (q, k, v))
+            o, _ = oracle.varlen_attention(qp, kp, vp, sub_cu)
+            out[rows] = o
+            t1, ru1 = time.perf_counter(), resource.getrusage(resource.RUSAGE_SELF)
+            threads = _cpu_threads(ru0, ru1, t1 - t0)
+            job += (t1 - t0) * sizes.size / windows_per_layer
+        if i >= args.warmup:
+            times.append(job)
+    sec = float(np.mean(times))
+    config = {"workload": wl.name, "tokens": wl.num_tokens, "heads": H, "head_dim": D,
+              "windows_sampled_per_layer": windows_per_layer}
+    sample = (f"per step {windows_per_layer} windows of each layer drawn uniformly: fp64 pack, attention and "
+              "restore of their rows, each layer's time scaled by its window count")
+    print(json.dumps(_reference_line(args, "shifted 3D window attention TFLOP/s (2 layers, attention in place "
+                                     "on the grid)", total_flops / sec / 1e12, UNIT, True, sec * 1e3, config,
+                                     threads, sample)), flush=True)
+
+
 def run_reference(args, rank, world):
     if rank != 0:
+        return
+    if args.workload in ("tiny_example", "single_request_4k"):
+        return _reference_full_packed(args)
+    if args.workload == "window_grid":
+        return _reference_window(args)
+    if args.workload != "h3_full_request":
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle is timed on h3_full_request, "
+                          "single_request_4k, tiny_example and window_grid only"}), flush=True)
         return
     from workloads import h3_full_request
 
