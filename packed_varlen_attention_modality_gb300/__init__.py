@@ -11,7 +11,8 @@ Calls:
   window_count / window_pack / window_unpack   shifted 3D window partition and row gather/scatter
   window_attn_fwd   shifted 3D window attention read and written in place on the grid
   vsa_select / vsa_attn_fwd   block-sparse video attention: block gate scores + top-k
-                    selection, then attention over the selected 64-token blocks
+                    selection, then attention over the selected 64-token blocks (paired query
+                    blocks share the key blocks both selected)
   continuation_plan / continuation_pack / continuation_append / masked_row_update
                     continuation window: tails, five row groups, overlap discard, target updates
   sp_assign_windows / sp_rank_tokens / sp_layer_order / sp_exchange_plan
