@@ -195,3 +195,33 @@ def test_row_subset_matches_full():
     assert np.allclose(os_[rows], o[rows], rtol=0, atol=1e-14)
     assert np.allclose(lses[:, rows], lse[:, rows], rtol=0, atol=1e-14)
     assert np.isnan(os_[1]).all()
+
+
+def test_a_repeated_block_counts_its_keys_twice():
+    """Listing a block twice doubles the weight of each of its keys.  With every block of a list
+    repeated, numerator and denominator double: the output is unchanged and the LSE grows by
+    exactly ln 2.  With one block of [a, b] repeated, the result equals attention over [a, b]
+    whose scores on a's keys are raised by ln 2 (a pure-Python masked softmax)."""
+    grid, block = (4, 4, 8), (2, 2, 4)   # 2 x 2 x 2 = 8 blocks of 16 tokens
+    N, H, D = 128, 1, 4
+    q, k, v = (_normal(s, (N, H, D)) for s in (31, 32, 33))
+    nblk = oracle.vsa_block_count(grid, block)
+    ids = oracle.vsa_block_ids(grid, block)
+    once = np.tile(np.array([1, 5]), (H, nblk, 1))
+    twice = np.tile(np.array([1, 1, 5, 5]), (H, nblk, 1))
+    o1, lse1 = oracle.vsa_attention(q, k, v, grid, block, once)
+    o2, lse2 = oracle.vsa_attention(q, k, v, grid, block, twice)
+    assert np.allclose(o2, o1, rtol=0, atol=1e-12)
+    assert np.allclose(lse2, lse1 + math.log(2.0), rtol=0, atol=1e-12)
+    # [1, 1, 5]: block 1's keys weigh double
+    o3, lse3 = oracle.vsa_attention(q, k, v, grid, block, np.tile(np.array([1, 1, 5]), (H, nblk, 1)))
+    keys = np.concatenate([np.nonzero(ids == 1)[0], np.nonzero(ids == 5)[0]])
+    bonus = np.where(ids[keys] == 1, math.log(2.0), 0.0)
+    for i in (0, 37, 127):
+        s = [sum(q[i, 0, d] * k[j, 0, d] for d in range(D)) / math.sqrt(D) + b for j, b in zip(keys, bonus)]
+        m = max(s)
+        w = [math.exp(x - m) for x in s]
+        z = sum(w)
+        ref = [sum(wi * v[j, 0, d] for wi, j in zip(w, keys)) / z for d in range(D)]
+        assert np.allclose(o3[i, 0], ref, rtol=0, atol=1e-12)
+        assert abs(lse3[0, i] - (m + math.log(z))) < 1e-12
