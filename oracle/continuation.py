@@ -11,7 +11,7 @@ s * 40 / 24 before RoPE (s = the window's first frame, 24 FPS video, 40 Hz audio
 part of the new samples that overlaps the reference rows in time is discarded and only the
 non-overlapping suffix is appended to the clip.
 
-Readings where the pages leave a step open (each listed in the design doc):
+Readings where the pages leave a step open:
   * Units.  Video latents have `frames_per_latent` video frames (24 FPS) per latent frame
     (4 makes the H3 request's 29 latent frames and 200 audio rows one 5 s window); audio latents
     are 40 Hz rows.  The new window starts where the video tail starts: g0 = clip_frames - 7

@@ -12,7 +12,7 @@ Sources:
       video); only the time axis moves, spatial coordinates stay; decimals are kept
       (start frame 238 -> 396.67).
 
-Readings where the pages are silent (each one also listed in the design doc):
+Readings where the pages are silent:
   * Rotation: pairs (x[2i], x[2i+1]) rotated by angle phi_i, as in the original RoFormer
     formulation:  x'[2i] = x[2i] cos phi - x[2i+1] sin phi,  x'[2i+1] = x[2i] sin phi + x[2i+1] cos phi.
   * Frequency ladder of a band of width d: theta_i = base^(-2i/d), i in [0, d/2).

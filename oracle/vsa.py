@@ -6,7 +6,7 @@ Source: [H3-fast] "Breaking the engineering bottlenecks of video-generation mode
 top-k blocks; fine attention at token level between the selected blocks only).  The pages do not
 give the top-k ratio.
 
-Readings where the pages leave a step open (each listed in the design doc):
+Readings where the pages leave a step open:
   * Blocks: the (T, H, W) latent grid is cut into (bt, bh, bw) = (4, 4, 4) cubes along each axis
     starting at 0, without shift; a token at (t, h, w) is in block (t // bt, h // bh, w // bw);
     edge blocks are cropped by the grid.  Block id is lexicographic (i_t, i_h, i_w).

@@ -6,7 +6,7 @@ that neighbouring windows' boundary tokens meet; windows at the grid edge are in
 ("cropped", of unequal size); after attention the scattered tokens are put back in their
 original order.
 
-Readings (also listed in the design doc):
+Readings of the pages taken here:
   * Along an axis of length L with window w and shift s, token x belongs to axis window
     floor((x + s) / w); there are ceil((L + s) / w) axis windows; when s > 0 the first is
     w - s wide and the last is cropped by the grid edge.  Edge windows are cropped, not rolled
