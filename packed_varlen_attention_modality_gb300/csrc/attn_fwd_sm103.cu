@@ -58,6 +58,8 @@
 // wait's parity from them; no waiter can fall more than one phase behind its barrier.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include <type_traits>
 
 #include "h3_internal.h"
@@ -1136,30 +1138,32 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
 }
 
 int num_sms_of_current_device() {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64];  // 0 until looked up; racing lookups store the same value
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 template <int D, int kMode>
 cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
   using C = Cfg<D, kMode>;
-  static bool configured[64] = {};  // the shared-memory opt-in is made once per device
+  // the shared-memory opt-in is made once per device (a second call from a racing thread is
+  // harmless; the flags are atomic so the race is defined)
+  static std::atomic<bool> configured[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
+  if (!configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(attn_fwd_kernel<D, kMode>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_release);
   }
   const int sms = num_sms_of_current_device();
   if (sms <= 0) return cudaErrorInvalidDevice;

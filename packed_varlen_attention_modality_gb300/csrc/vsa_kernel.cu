@@ -28,6 +28,8 @@
 // list entry.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include <cstdint>
 
 #include "h3_internal.h"
@@ -341,16 +343,18 @@ vsa_schedule_kernel(const int32_t* __restrict__ sel, int nblk, int heads, int to
 template <int D>
 cudaError_t launch_score(dim3 grid, const float* qm, const float* km, int nblk, float scale,
                          float* scores, cudaStream_t stream) {
-  static bool configured[64] = {};  // the shared-memory opt-in is made once per device
+  // the shared-memory opt-in is made once per device (a second call from a racing thread is
+  // harmless; the flags are atomic so the race is defined)
+  static std::atomic<bool> configured[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
+  if (!configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(vsa_score_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              score_smem_bytes<D>());
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_release);
   }
   vsa_score_kernel<D><<<grid, kScoreThreads, score_smem_bytes<D>(), stream>>>(qm, km, nblk, scale,
                                                                               scores);
