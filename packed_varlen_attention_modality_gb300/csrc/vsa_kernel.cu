@@ -10,9 +10,9 @@
 //
 // Three kernels, all HBM- or FFMA-bound (the gate is ~1 % of the fine attention's work):
 //   vsa_pool_kernel    mean of each block's Q and K rows per head (fp32 sums in token order)
-//   vsa_score_kernel   S_h = scale * Qmean_h Kmean_h^T, a 64 x 256 output tile per CTA with
-//                      8 x 8 register micro-tiles (two broadcast and two float4 shared loads per
-//                      64 FFMA), written to the caller's [H, nblk, nblk] score buffer
+//   vsa_score_kernel   S_h = scale * Qmean_h Kmean_h^T, a 64 x 128 output tile per CTA with
+//                      8 x 4 register micro-tiles (two broadcast and one float4 shared loads per
+//                      32 FFMA), written to the caller's [H, nblk, nblk] score buffer
 //   vsa_topk_kernel    one warp per (head, query block): 8-bit radix select of the k-th largest
 //                      score over 4 passes (the row stays in L1/L2), then an ascending ballot
 //                      compaction that takes the ties at the threshold lowest id first
@@ -40,7 +40,7 @@ namespace {
 
 constexpr int kPoolThreads = 256;
 constexpr int kScoreRows = 64;     // query blocks per score tile
-constexpr int kScoreCols = 256;    // key blocks per score tile
+constexpr int kScoreCols = 128;    // key blocks per score tile
 constexpr int kScoreThreads = 256;
 constexpr int kTopkWarps = 8;
 constexpr int kSchedWarps = 8;
@@ -97,10 +97,11 @@ vsa_pool_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   }
 }
 
-// grid (ceil(nblk / 256), ceil(nblk / 64), heads).  Thread (rg, kg) = (tid / 32, tid % 32)
-// computes query blocks 8 rg .. 8 rg + 7 against key blocks 4 kg .. 4 kg + 3 and
-// 128 + 4 kg .. 128 + 4 kg + 3 of the tile: per dimension two broadcast and two conflict-free
-// float4 shared loads feed 64 FFMA, so the FMA pipes, not shared memory, set the pace.
+// grid (ceil(nblk / 128), ceil(nblk / 64), heads).  Thread (rg, kg) = (tid / 32, tid % 32)
+// computes query blocks 8 rg .. 8 rg + 7 against key blocks 4 kg .. 4 kg + 3 of the tile: per
+// dimension two broadcast and one conflict-free float4 shared load feed 32 FFMA.  The tile's
+// operands (102 KB at D = 128) leave room for two CTAs per SM, so one CTA's loads overlap the
+// other's FFMA (a 64 x 256 tile, one CTA per SM, kept the FMA pipes 27 % busy).
 constexpr int kQs = kScoreRows + 4;  // padded smem row lengths (float4 alignment kept)
 constexpr int kKs = kScoreCols + 4;
 template <int D>
@@ -129,19 +130,18 @@ vsa_score_kernel(const float* __restrict__ qm, const float* __restrict__ km, int
   }
   __syncthreads();
   const int rg = threadIdx.x >> 5, kg = threadIdx.x & 31;
-  float acc[8][8] = {};
+  float acc[8][4] = {};
 #pragma unroll 4
   for (int d = 0; d < D; ++d) {
     const float4 a0 = *reinterpret_cast<const float4*>(&qs[d * kQs + 8 * rg]);
     const float4 a1 = *reinterpret_cast<const float4*>(&qs[d * kQs + 8 * rg + 4]);
     const float4 b0 = *reinterpret_cast<const float4*>(&ks[d * kKs + 4 * kg]);
-    const float4 b1 = *reinterpret_cast<const float4*>(&ks[d * kKs + 128 + 4 * kg]);
     const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const float bv[4] = {b0.x, b0.y, b0.z, b0.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+      for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -149,8 +149,8 @@ vsa_score_kernel(const float* __restrict__ qm, const float* __restrict__ km, int
     if (r >= nblk) break;
     float* row = scores + (static_cast<size_t>(h) * nblk + r) * nblk;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int c = c0 + (j < 4 ? 4 * kg + j : 128 + 4 * kg + (j - 4));
+    for (int j = 0; j < 4; ++j) {
+      const int c = c0 + 4 * kg + j;
       if (c < nblk) row[c] = acc[i][j] * scale;
     }
   }
