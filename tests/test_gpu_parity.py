@@ -373,7 +373,13 @@ def test_window_attention_in_place_matches_oracle_and_packed_path(h3, dev, windo
 @pytest.mark.parametrize("grid,win,shift", [((5, 9, 11), (4, 8, 8), (2, 4, 4)),
                                             ((3, 16, 8), (2, 8, 8), (1, 4, 0)),
                                             ((6, 7, 5), (4, 4, 8), (0, 2, 3)),
-                                            ((7, 9, 20), (3, 4, 16), (1, 2, 8))])
+                                            ((7, 9, 20), (3, 4, 16), (1, 2, 8)),
+                                            # odd window height (no half-height maps), one-tile
+                                            # windows of 4 frames, cropped frames and columns
+                                            ((5, 3, 70), (4, 1, 32), (2, 0, 16)),
+                                            # a window wider than the grid: most of every box
+                                            # lies outside it; height-2 edge boxes of height 1
+                                            ((9, 6, 10), (2, 2, 64), (1, 1, 0))])
 def test_window_attention_in_place_small_grids_full_oracle(h3, dev, D, grid, win, shift):
     n = grid[0] * grid[1] * grid[2]
     rng = np.random.default_rng(n + D)
