@@ -8,7 +8,8 @@ audio 200 + video 29x40x50), 40 heads x 128, bf16, segments [0,558,758,58758], c
 with NaN pad rows.  Metric: attention TFLOP/s = 4*H*D*sum(n_g^2) / step time.
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU fp64 oracle instead (the only
-reference that exists for this method), on a bounded sample of the same workload.
+reference that exists for this method): on a bounded sample of the H3 request or of the window
+layer pair, or in full for the worked example and the 4,096-token request.
 """
 from __future__ import annotations
 
@@ -30,7 +31,6 @@ if ROOT not in sys.path:
 
 METRIC = "packed varlen attn TFLOP/s @58,758 tok, 40x128 bf16; % GB300 dense BF16 peak"
 UNIT = "TFLOP/s"
-L2_BYTES = 129 * 2 ** 20
 
 
 def parse_args():
