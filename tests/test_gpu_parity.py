@@ -193,6 +193,25 @@ def test_edge_lengths_against_oracle(h3, dev, D, lengths):
     assert torch.all(o[N:] == 3.0) and torch.all(lse[:, N:] == 5.0)
 
 
+def test_maximum_segment_count_against_oracle(h3, dev):
+    """65,535 segments (the most the call accepts) of 0 to 4 rows each: the plan lists far more
+    segments than it orders longest-first, most items hold a single short query tile, and the
+    empty segments produce nothing."""
+    lengths = [int(x) for x in np.random.default_rng(29).integers(0, 5, 65535)]
+    wl = W.random_packed(29, lengths, heads=1, head_dim=64, capacity=sum(lengths) + 7)
+    d = _to(dev, wl)
+    o = torch.full_like(d["q"], 3.0)
+    lse = torch.full((1, wl.capacity), 5.0, device=dev)
+    h3.varlen_attn_fwd(d["q"], d["k"], d["v"], d["cu"], max(1, wl.max_seqlen), out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert h3.get_device_error(dev) == 0
+    N = wl.num_tokens
+    ref_o, ref_lse = oracle.varlen_attention(wl.q, wl.k, wl.v, wl.cu_seqlens)
+    _close(o[:N].float().cpu().numpy(), ref_o[:N], "65,535 segments")
+    _lse_close(lse[:, :N].cpu().numpy(), ref_lse[:, :N], "65,535 segments")
+    assert torch.all(o[N:] == 3.0) and torch.all(lse[:, N:] == 5.0)
+
+
 def test_explicit_softmax_scale(h3, dev):
     wl = W.random_packed(7, [300, 45], heads=2, head_dim=128)
     d = _to(dev, wl)
