@@ -26,7 +26,7 @@ routines, brute force and the pages' printed examples.  Readings where the pages
 are listed in the module docstrings of ``rope`` and ``window``.
 """
 from .attention import varlen_attention, attention_weights, dense_masked_attention_bruteforce
-from .rope import (continuation_time_shift, rope_inv_freq, rope_angles, rope_apply,
+from .rope import (RopeConfig, continuation_time_shift, rope_inv_freq, rope_angles, rope_apply,
                    video_axis_split)
 from .window import (axis_window_count, window_count, window_ids, window_partition,
                      window_pack, window_unpack)
@@ -37,7 +37,8 @@ from .vsa import (vsa_block_counts, vsa_block_count, vsa_block_ids, vsa_block_me
 
 __all__ = [
     "varlen_attention", "attention_weights", "dense_masked_attention_bruteforce",
-    "continuation_time_shift", "rope_inv_freq", "rope_angles", "rope_apply", "video_axis_split",
+    "RopeConfig", "continuation_time_shift", "rope_inv_freq", "rope_angles", "rope_apply",
+    "video_axis_split",
     "axis_window_count", "window_count", "window_ids", "window_partition", "window_pack",
     "window_unpack", "vsa_block_counts", "vsa_block_count", "vsa_block_ids", "vsa_block_means",
     "vsa_block_scores", "vsa_select", "vsa_attention", "ContinuationPlan", "continuation_plan",

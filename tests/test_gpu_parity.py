@@ -117,6 +117,32 @@ def test_rope_parity(packed_case):
         _close(t_out[rows].float().numpy(), ref, f"{name} rope")
 
 
+@pytest.mark.parametrize("D,dims", [(128, (32, 48, 48)), (64, (16, 24, 24))])
+def test_rope_custom_config_against_oracle(h3, dev, D, dims):
+    """Non-default RoPE settings: a base per modality, a video band split other than D/2:D/4:D/4
+    and other sample rates in the continuation shift (s * audio_hz / video_fps), with two
+    requests whose start frames differ."""
+    wl = W.random_packed(41 + D, [60, 200, 90, 150], heads=2, head_dim=D, capacity=520)
+    N = wl.num_tokens
+    cu_req = np.array([0, 260, N], np.int32)
+    frames = np.array([17.0, 330.0], np.float32)
+    cfg_h = h3.RopeConfig(base_text=5000.0, base_video=20000.0, base_audio=1000.0,
+                          video_dims_t=dims[0], video_dims_h=dims[1], video_dims_w=dims[2],
+                          audio_hz=48.0, video_fps=25.0)
+    cfg_o = oracle.RopeConfig(base_text=5000.0, base_video=20000.0, base_audio=1000.0,
+                              video_dims_t=dims[0], video_dims_h=dims[1], video_dims_w=dims[2],
+                              audio_hz=48.0, video_fps=25.0)
+    d = _to(dev, wl)
+    qo, ko = h3.rope_apply(d["q"], d["k"], d["pos"], d["tag"], torch.from_numpy(cu_req).to(dev),
+                           torch.from_numpy(frames).to(dev), num_tokens=N,
+                           q_out=torch.empty_like(d["q"]), k_out=torch.empty_like(d["k"]), cfg=cfg_h)
+    torch.cuda.synchronize()
+    assert h3.get_device_error(dev) == 0
+    for got, src in ((qo, wl.q), (ko, wl.k)):
+        ref = oracle.rope_apply(src, wl.pos, wl.tag, cu_req, frames, cfg=cfg_o, num_tokens=N)
+        _close(got[:N].float().cpu().numpy(), ref[:N], f"rope custom config D {D}")
+
+
 def test_attention_parity_on_gpu_rope_output(packed_case):
     """Parity (i): attention alone, the oracle fed the GPU's own bf16 RoPE outputs."""
     name, r = packed_case
