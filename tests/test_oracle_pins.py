@@ -414,3 +414,92 @@ def test_rope_row_subset_matches_full():
     rows = np.array([3, 15, 19, 20, 44])
     sub = oracle.rope_apply(wl.q, wl.pos, wl.tag, [0, 20, 45], [0.0, 119.0], rows=rows)
     assert np.array_equal(sub, full[rows])
+
+
+# ----------------------------------------------------------------------------------------------
+# non-default RoPE configuration: a base per modality, an uneven video band split, other rates
+# in the continuation shift ([H3-vLLM] §3: the tag selects the frequencies)
+# ----------------------------------------------------------------------------------------------
+
+# bases whose square roots are whole numbers, so a quarter turn of the pair at index d/4 of a
+# band (theta = base^(-1/2)) falls at a coordinate that is a simple multiple of pi
+CUSTOM_BASES = dict(base_text=2500.0, base_video=900.0, base_audio=400.0)  # sqrt 50, 30, 20
+CUSTOM_SPLIT = (24, 64, 40)  # three different widths at D = 128: t, h, w
+
+
+def _custom_cfg(**kw):
+    return oracle.RopeConfig(**CUSTOM_BASES, video_dims_t=CUSTOM_SPLIT[0], video_dims_h=CUSTOM_SPLIT[1],
+                             video_dims_w=CUSTOM_SPLIT[2], **kw)
+
+
+def _unit_pairs(n, D):
+    x = np.zeros((n, 1, D))
+    x[:, 0, 0::2] = 1.0  # every pair starts at (1, 0)
+    return x
+
+
+def test_custom_bases_quarter_turn_at_a_quarter_of_each_ladder():
+    """Pair D/4 of a text / audio row turns by t * base^(-1/2): a quarter turn at t = sqrt(base) pi/2.
+    With distinct bases a swapped base_text / base_audio (or video) turns by another angle."""
+    D = 128
+    cfg = _custom_cfg()
+    x = _unit_pairs(3, D)
+    pos = np.zeros((3, 3), np.float64)
+    pos[0, 0] = 25.0 * math.pi   # text:  sqrt(2500) = 50 -> 25 pi / 50 = pi / 2
+    pos[1, 0] = 10.0 * math.pi   # audio: sqrt(400)  = 20 -> 10 pi / 20 = pi / 2
+    pos[2, 0] = 6.0 * math.pi    # video time band (24 dims): pair 6 turns by 6 pi / 30 ... see below
+    tag = np.array([TAG_TEXT, TAG_AUDIO, TAG_VIDEO], np.uint8)
+    y = oracle.rope_apply(x, pos, tag, cfg=cfg)
+    for r in (0, 1):  # pair D/4 = 32 -> dims 64, 65 at (0, 1)
+        assert abs(y[r, 0, 64]) < 1e-12 and abs(y[r, 0, 65] - 1.0) < 1e-12, r
+    # video time band of width 24: its pair 24/4 = 6 (dims 12, 13) has theta = 900^(-1/2) = 1/30,
+    # so t = 6 pi turns it by pi / 5; its pair 0 (theta = 1) turns by 6 pi = a whole number of turns
+    assert abs(y[2, 0, 12] - math.cos(math.pi / 5)) < 1e-12 and abs(y[2, 0, 13] - math.sin(math.pi / 5)) < 1e-12
+    assert abs(y[2, 0, 0] - 1.0) < 1e-12 and abs(y[2, 0, 1]) < 1e-12
+    # the pair just before a band's quarter point is not at the special angle (the ladder is
+    # anchored per band, not per head)
+    assert abs(y[0, 0, 62]) > 1e-3
+
+
+def test_custom_video_split_bands_move_only_their_dims_and_restart():
+    """Split 24 / 64 / 40: moving t, h or w changes exactly dims [0,24), [24,88), [88,128), the
+    first pair of each band (theta = 1) is negated by a half turn, and the pair at a quarter of
+    each band turns by coordinate * 900^(-1/2)."""
+    D = 128
+    cfg = _custom_cfg()
+    dt, dh, dw = oracle.video_axis_split(D, *CUSTOM_SPLIT)
+    assert (dt, dh, dw) == CUSTOM_SPLIT
+    bands = [(0, dt), (dt, dt + dh), (dt + dh, D)]
+    x = np.random.default_rng(11).standard_normal((1, 1, D))
+    tag = np.array([TAG_VIDEO], np.uint8)
+    y0 = oracle.rope_apply(x, np.zeros((1, 3)), tag, cfg=cfg)
+    assert np.array_equal(y0, x)
+    for axis, (lo, hi) in enumerate(bands):
+        p = np.zeros((1, 3))
+        p[0, axis] = math.pi
+        y = oracle.rope_apply(x, p, tag, cfg=cfg)
+        changed = np.nonzero(np.abs(y - x)[0, 0] > 1e-12)[0]
+        assert changed.min() == lo and changed.max() == hi - 1, axis
+        assert abs(y[0, 0, lo] + x[0, 0, lo]) < 1e-12 and abs(y[0, 0, lo + 1] + x[0, 0, lo + 1]) < 1e-12
+        # quarter turn of the band's pair (hi - lo) / 4 at coordinate 15 pi (15 pi / 30 = pi / 2)
+        u = _unit_pairs(1, D)
+        p[0, axis] = 15.0 * math.pi
+        yu = oracle.rope_apply(u, p, tag, cfg=cfg)
+        k = lo + 2 * ((hi - lo) // 4)
+        assert abs(yu[0, 0, k]) < 1e-12 and abs(yu[0, 0, k + 1] - 1.0) < 1e-12, axis
+
+
+def test_custom_shift_rates_closed_form():
+    """s * audio_hz / video_fps with other rates: 330 * 48 / 25 = 633.6, and a start frame of
+    25 pi / 48 at 48 / 25 moves t by exactly pi (pair 0 of a text row at t = 0 is negated); with
+    the rates swapped it would move by 25^2 pi / 48^2."""
+    cfg = _custom_cfg(audio_hz=48.0, video_fps=25.0)
+    assert oracle.continuation_time_shift(330.0, cfg.audio_hz, cfg.video_fps) == float(Fraction(330 * 48, 25))
+    off = oracle.rope.request_time_offsets(4, [0, 2, 4], [0.0, 330.0], cfg)
+    assert np.array_equal(off, [0.0, 0.0, float(Fraction(330 * 48, 25)), float(Fraction(330 * 48, 25))])
+    x = _unit_pairs(2, 128)
+    pos = np.zeros((2, 3))
+    tag = np.array([TAG_TEXT, TAG_TEXT], np.uint8)
+    y = oracle.rope_apply(x, pos, tag, [0, 1, 2], [0.0, 25.0 * math.pi / 48.0], cfg=cfg)
+    assert np.array_equal(y[0], x[0])                     # request 0: no shift
+    assert abs(y[1, 0, 0] + 1.0) < 1e-12 and abs(y[1, 0, 1]) < 1e-12
