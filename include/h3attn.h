@@ -31,6 +31,10 @@
  *     the kernel skip the affected work and record an error code in the device error word,
  *     never access memory out of bounds.  h3_get_device_error() reads (and clears) that word.
  *   - No exceptions cross the ABI; nothing aborts; no device trap.
+ *   - The library looks up the device addresses of its own device variables (the error word,
+ *     the array of h3_varlen_attn_fwd_noalloc) once per device and keeps them for the life of
+ *     the process.  Do not use it across a cudaDeviceReset (or any other destruction of a
+ *     device's primary context): the variables would then live at new addresses.
  */
 #ifndef H3ATTN_H_
 #define H3ATTN_H_

@@ -81,7 +81,7 @@ constexpr int kColS = 256;            // S / P of tile t at kColS + 128 t
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the running max grows by > 2^8
 constexpr int kPlanThreads = 1024;
 constexpr int kSortMax = 256;         // segments ordered longest-first up to this count
-constexpr int kWsHeader = 4;          // workspace words: (spare), total items, 2 spare
+constexpr int kWsHeader = kAttnWsHeaderWords;  // workspace words: (spare), total items, 2 spare
 constexpr int kPersistMaxSeqlen = 2048;  // loop over items per CTA up to this segment length
 
 constexpr int kModePacked = kAttnModePacked;  // kernel variants (see h3_internal.h)
@@ -89,11 +89,6 @@ constexpr int kModeWindow = kAttnModeWindow;
 constexpr int kModeVsa = kAttnModeVsa;
 constexpr int kVsaBlockRows = 64;  // rows of one VSA block = half a 128-row tile
 
-// Workspace (uint32 words): [1] total items, [kWsHeader, +S) segment order,
-// [kWsHeader + S, +S+1) exclusive prefix of items in that order.
-__host__ __device__ constexpr size_t workspace_words(int num_segments) {
-  return kWsHeader + 2 * static_cast<size_t>(num_segments) + 1;
-}
 
 struct WorkDesc {
   int seg_start;  // packed: first row of the segment
@@ -1217,10 +1212,6 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-size_t attn_workspace_bytes(int num_segments) {
-  const size_t bytes = workspace_words(num_segments) * sizeof(uint32_t);
-  return (bytes + 255) / 256 * 256;
-}
 
 cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t stream) {
   if (a.mode == kModeWindow) {

@@ -92,7 +92,14 @@ struct AttnArgs {
   unsigned int* err;
 };
 
-size_t attn_workspace_bytes(int num_segments);
+// Workspace of the packed variant (uint32 words): [1] total items, [kAttnWsHeaderWords, +S)
+// segment order, [kAttnWsHeaderWords + S, +S+1) exclusive prefix of items in that order; the
+// byte count is rounded up to 256.
+constexpr int kAttnWsHeaderWords = 4;
+constexpr size_t attn_workspace_bytes(int num_segments) {
+  return ((kAttnWsHeaderWords + 2 * static_cast<size_t>(num_segments) + 1) * sizeof(uint32_t) + 255) /
+         256 * 256;
+}
 cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t stream);
 
 // ---- VSA block gate + top-k ----------------------------------------------------------------

@@ -20,6 +20,8 @@
 // enough for H3_NOALLOC_MAX_SEGMENTS segments) until the process exits.  It is shared by all
 // calls on a device.
 constexpr int kNoallocScratchBytes = 132 * 1024;
+static_assert(h3::attn_workspace_bytes(H3_NOALLOC_MAX_SEGMENTS) <= kNoallocScratchBytes,
+              "the no-alloc array must hold the plan of H3_NOALLOC_MAX_SEGMENTS segments");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 namespace {

@@ -47,7 +47,7 @@ __device__ __forceinline__ uint4 rotate4(uint4 x, const float2* __restrict__ cs)
 }
 
 __global__ void __launch_bounds__(kThreads)
-rope_kernel(const uint4* __restrict__ q_in, uint4* q_out, const uint4* k_in, uint4* k_out,
+rope_kernel(const uint4* q_in, uint4* q_out, const uint4* k_in, uint4* k_out,
             int num_tokens, int num_heads, int head_dim, const float* __restrict__ pos,
             const uint8_t* __restrict__ tag, const int32_t* __restrict__ cu_requests,
             int num_requests, const float* __restrict__ start_frames,

@@ -2,9 +2,10 @@
 
 Some callers cannot allocate device memory -- their memory is owned by an external pool or
 allocator, or a cudaMalloc there would stall or is not allowed -- so the library offers this
-variant that keeps its work plan in a fixed array of its own.  It must give the same results
-as h3_varlen_attn_fwd with a caller workspace, call after call (the shared array keeps the
-previous call's contents, which must not matter).
+variant that keeps its work plan in a fixed array of its own.  It runs the same plan kernel and
+the same attention kernel as h3_varlen_attn_fwd with a caller workspace, so on the same inputs
+its outputs must be the same bytes, call after call: the shared array keeps the previous call's
+plan, which must never leak into the next one.
 
 Kept in a file of its own that pytest collects last.
 """
@@ -18,7 +19,7 @@ import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-MAX_ABS, MEAN_ABS, LSE_REL = 2e-2, 2e-3, 1e-4  # the tolerances of the other GPU parity tests
+NOALLOC_MAX_SEGMENTS = 16384  # H3_NOALLOC_MAX_SEGMENTS
 
 
 @pytest.fixture(scope="module")
@@ -51,6 +52,7 @@ def _case(dev, wl):
     d = dict(q=wl.q.to(dev), k=wl.k.to(dev), v=wl.v.to(dev), cu=torch.from_numpy(wl.cu_seqlens).to(dev))
     d["C"], d["H"], d["D"] = wl.q.shape
     d["S"], d["maxs"] = wl.num_segments, max(1, wl.max_seqlen)
+    d["N"] = wl.num_tokens
     return d
 
 
@@ -75,19 +77,22 @@ def _no_alloc(lib, dev, c):
 
 
 def _same(got, ref, N, what):
+    """Same plan, same kernel, same inputs: the same bytes (pad rows untouched on both sides)."""
     o, lse = got
     o_ref, lse_ref = ref
-    err = (o[:N].float() - o_ref[:N].float()).abs()
-    assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS, what
-    rel = (lse[:, :N] - lse_ref[:, :N]).abs() / lse_ref[:, :N].abs().clamp_min(1.0)
-    assert rel.max().item() <= LSE_REL, what
-    assert torch.all(o[N:] == 5.0) and torch.all(lse[:, N:] == 5.0), what  # pad rows untouched
+    assert torch.equal(o, o_ref), f"{what}: output differs"
+    assert torch.equal(lse, lse_ref), f"{what}: lse differs"
+    assert torch.all(o[N:] == 5.0) and torch.all(lse[:, N:] == 5.0), what
 
 
 def test_no_alloc_matches_workspace_entry_point_on_consecutive_calls(lib, dev):
+    # each case follows one of another shape, so a plan left in the array by the previous call
+    # (more segments, longer segments) would show if anything read it
     cases = [W.random_packed(31, [300, 1, 517, 0, 1024, 129], heads=4, head_dim=128, capacity=2048),
              W.tiny_example(capacity=64),
-             W.random_packed(32, [256] * 40 + [77, 3], heads=2, head_dim=128, capacity=10400)]
+             W.random_packed(32, [256] * 40 + [77, 3], heads=2, head_dim=128, capacity=10400),
+             W.random_packed(33, [2500, 40, 3], heads=3, head_dim=64, capacity=2600),
+             W.tiny_example(capacity=64)]
     for wl in cases:
         c = _case(dev, wl)
         ref = _with_workspace(lib, dev, c)
@@ -95,12 +100,27 @@ def test_no_alloc_matches_workspace_entry_point_on_consecutive_calls(lib, dev):
         second = _no_alloc(lib, dev, c)  # the array still holds the first call's plan
         torch.cuda.synchronize()
         assert lib.h3_get_device_error(_stream(dev)) == 0
-        _same(first, ref, wl.num_tokens, f"{wl.name} first call")
-        _same(second, ref, wl.num_tokens, f"{wl.name} second call")
+        _same(first, ref, c["N"], f"{wl.name} first call")
+        _same(second, ref, c["N"], f"{wl.name} second call")
+
+
+def test_no_alloc_at_its_segment_limit(lib, dev):
+    """Exactly H3_NOALLOC_MAX_SEGMENTS segments of 0-5 rows: the largest plan the array holds,
+    and more segments than the plan orders longest-first (its unsorted branch)."""
+    lengths = [int(x) for x in np.random.default_rng(34).integers(0, 6, NOALLOC_MAX_SEGMENTS)]
+    wl = W.random_packed(34, lengths, heads=2, head_dim=64, capacity=sum(lengths) + 9)
+    c = _case(dev, wl)
+    assert c["S"] == NOALLOC_MAX_SEGMENTS
+    ref = _with_workspace(lib, dev, c)
+    for call in ("first", "second"):
+        got = _no_alloc(lib, dev, c)
+        torch.cuda.synchronize()
+        assert lib.h3_get_device_error(_stream(dev)) == 0
+        _same(got, ref, c["N"], f"{NOALLOC_MAX_SEGMENTS} segments, {call} call")
 
 
 def test_no_alloc_refuses_more_segments_than_its_array_holds(lib, dev):
-    limit = 16384  # H3_NOALLOC_MAX_SEGMENTS
+    limit = NOALLOC_MAX_SEGMENTS
     q = torch.zeros(64, 1, 64, dtype=torch.bfloat16, device=dev)
     cu = torch.zeros(limit + 2, dtype=torch.int32, device=dev)
     st = lib.h3_varlen_attn_fwd_noalloc(_p(q), _p(q), _p(q), _p(q), None, _p(cu), limit + 1, 1, 64, 1, 64,
