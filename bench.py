@@ -41,6 +41,10 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other workloads' short measurements after the headline")
+    p.add_argument("--config-steps", type=int, default=5,
+                   help="timed steps of each other workload measured after the headline")
     p.add_argument("--workload", default="h3_full_request",
                    choices=["h3_full_request", "single_request_4k", "continuation_batch",
                             "continuation_batch_4seg",
@@ -118,7 +122,7 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.reader.join(timeout=2)
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             parts = [x.strip() for x in line.split(",")]
@@ -129,12 +133,21 @@ class ClockSampler:
                 smax.append(float(parts[2]))
             except ValueError:
                 continue
+            try:
+                power.append(float(parts[3]))
+            except ValueError:
+                power.append(float("nan"))
             for name, val in zip(names, parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
+        # samples under load: power draw at least half of the highest seen in the window
+        pw = np.array(power, dtype=np.float64)
+        loaded = [c for c, w in zip(sm, pw) if np.isfinite(w) and w >= 0.5 * np.nanmax(pw)] if sm else []
         return {"sm_mhz": float(np.median(sm)) if sm else None,
                 "sm_max_mhz": float(max(smax)) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "sm_mhz_loaded": float(np.median(loaded)) if loaded else None,
+                "power_w_max": float(np.nanmax(pw)) if sm else None,
+                "reasons": sorted(reasons), "samples": len(sm), "samples_loaded": len(loaded)}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -317,24 +330,46 @@ def run_reference(args, rank, world):
 # ------------------------------------------------------------------------------------------------
 # our arm
 # ------------------------------------------------------------------------------------------------
+# dense bf16 tcgen05 work per SM per cycle: one 128 x 128 x 16 MMA (524,288 FLOP) every 64 cycles
+# (measured on this GPU with a sequence of such MMAs issued back to back)
+TENSOR_FLOP_PER_SM_CYCLE = 8192.0
+
+
 def run_ours(args, rank, world, local_rank):
     import packed_varlen_attention_modality_gb300 as h3
-    import workloads
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     h3.load_library()
     peaks = load_peaks()
     if args.workload.startswith("window_grid"):
-        return run_window(args, rank, world, dev, h3, peaks)
-    if args.workload.startswith("vsa_video"):
-        return run_vsa(args, rank, world, dev, h3, peaks)
-    if args.workload == "continuation_window":
-        return run_continuation(args, rank, world, dev, h3, peaks)
-    if args.workload == "tiny_example":
-        return run_latency(args, rank, world, dev, h3)
+        line = run_window(args, rank, world, dev, h3, peaks)
+    elif args.workload.startswith("vsa_video"):
+        line = run_vsa(args, rank, world, dev, h3, peaks)
+    elif args.workload == "continuation_window":
+        line = run_continuation(args, rank, world, dev, h3, peaks)
+    elif args.workload == "tiny_example":
+        line = run_latency(args, rank, world, dev, h3)
+    else:
+        line = run_packed(args, rank, world, dev, h3, peaks)
+    if args.workload == "h3_full_request" and not args.no_configs:
+        if world == 1:
+            line["configs"] = collect_configs(args, rank, world, dev, h3, peaks)
+        else:
+            line["configs"] = {"skipped": "the other workloads are measured at one GPU only"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_packed(args, rank, world, dev, h3, peaks, wl=None):
+    """One packed request per step: tagged RoPE of Q and K (with the continuation shift), then
+    block-diagonal attention over cu_seqlens.  The headline workload also gets the end-to-end leg
+    and the CPU baseline."""
+    import workloads
+
     headline = args.workload == "h3_full_request"
-    wl = workloads.WORKLOADS[args.workload]()
+    if wl is None:
+        wl = workloads.WORKLOADS[args.workload]()
     H, D, C, N = wl.num_heads, wl.head_dim, wl.capacity, wl.num_tokens
     flops = wl.attention_flops()
 
@@ -368,7 +403,7 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError("device error during warm-up")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    sampler = ClockSampler(local_rank)
+    sampler = ClockSampler(dev.index)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
@@ -398,11 +433,17 @@ def run_ours(args, rank, world, local_rank):
     rope_gbs = rope_bytes / (rope_ms / 1e3) / 1e9
     traffic = None
     traffic_file = os.path.join(ROOT, "profiles", "attn_fwd_dram_traffic.json")
-    if os.path.exists(traffic_file):
+    if headline and os.path.exists(traffic_file):
         with open(traffic_file) as f:
             tj = json.load(f)
         if tj.get("kernel_source_sha") == _kernel_sha():
             traffic = tj.get("dram_bytes_per_launch")
+    # tensor peak at the clock the kernel actually ran at (sampled, never set): SMs x per-SM rate
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    # (only when at least three samples fell under load: a timed region shorter than about a
+    # second gives the 200 ms sampler nothing to go on)
+    mhz = clocks.get("sm_mhz_loaded") if (clocks.get("samples_loaded") or 0) >= 3 else None
+    clock_peak = sms * TENSOR_FLOP_PER_SM_CYCLE * mhz * 1e6 / 1e12 if mhz else None
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -413,34 +454,103 @@ def run_ours(args, rank, world, local_rank):
     if headline and rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
 
-    if rank == 0:
-        line = {
-            "metric": METRIC if headline else f"packed varlen attn TFLOP/s ({wl.name})", "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.name, "tokens": N, "capacity": C, "heads": H, "head_dim": D,
-                       "cu_seqlens": [int(x) for x in wl.cu_seqlens], "attention_flop": flops,
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "inputs larger than L2 (each of Q, K, V, O is %.0f MB > 129 MB)"
-                             % (C * H * D * 2 / 1e6)},
-            "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": attn_tflops / peaks["bf16_tflops"],
-                         "traffic": traffic, "kernel": "attn_fwd_kernel<128>",
-                         "peak_source": peaks["source"] + " bf16_tflops (burst)",
-                         "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"],
-                         "attn_ms": attn_ms},
-            "kernels": {"rope": {"ms": rope_ms, "gbs": rope_gbs, "bytes": rope_bytes,
-                                 "frac_hbm": rope_gbs / peaks["hbm_gbs"]},
-                        "attn_fwd": {"ms": attn_ms, "tflops": attn_tflops,
-                                     "ms_median": float(np.median(attn_each)),
-                                     "ms_min": float(np.min(attn_each)),
-                                     "tflops_median": flops / (float(np.median(attn_each)) / 1e3) / 1e12}},
-            "clocks": clocks,
-            "gpu_launches": 3 * args.steps,   # RoPE, attention plan, attention per step
-            "e2e": e2e,
-            "cpu_baseline": cpu,
-        }
-        print(json.dumps(line), flush=True)
+    return {
+        "metric": METRIC if headline else f"packed varlen attn TFLOP/s ({wl.name})", "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "tokens": N, "capacity": C, "heads": H, "head_dim": D,
+                   "cu_seqlens": [int(x) for x in wl.cu_seqlens], "attention_flop": flops,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (each of Q, K, V, O is %.0f MB > 129 MB)"
+                         % (C * H * D * 2 / 1e6)},
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": attn_tflops / peaks["bf16_tflops"],
+                     "traffic": traffic, "kernel": "attn_fwd_kernel<%d>" % D,
+                     "peak_source": peaks["source"] + " bf16_tflops (burst)",
+                     "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"],
+                     "attn_ms": attn_ms,
+                     "peak_at_sampled_clock": clock_peak,
+                     "frac_at_sampled_clock": attn_tflops / clock_peak if clock_peak else None,
+                     "sampled_clock_basis": "%d SMs x %d FLOP/cycle (128x128x16 bf16 MMA per 64 "
+                                            "cycles) x median SM MHz under load" % (sms, TENSOR_FLOP_PER_SM_CYCLE)},
+        "kernels": {"rope": {"ms": rope_ms, "gbs": rope_gbs, "bytes": rope_bytes,
+                             "frac_hbm": rope_gbs / peaks["hbm_gbs"]},
+                    "attn_fwd": {"ms": attn_ms, "tflops": attn_tflops,
+                                 "ms_median": float(np.median(attn_each)),
+                                 "ms_min": float(np.min(attn_each)),
+                                 "tflops_median": flops / (float(np.median(attn_each)) / 1e3) / 1e12}},
+        "clocks": clocks,
+        "gpu_launches": 3 * args.steps,   # RoPE, attention plan, attention per step
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+
+
+def collect_configs(args, rank, world, dev, h3, peaks):
+    """Short timed measurements of the other workloads, each against its own bound, after
+    the headline: the 4,096-token request and the 4-request continuation batch (tensor), the
+    window layer pair in place and through pack/attention/unpack (HBM), block-sparse attention
+    at top 1/8 (useful and issued tensor work), the continuation window's row movement (HBM) and
+    the worked example's latency.  Few steps each, so the whole run stays within minutes."""
+    import workloads
+
+    def sub(name):
+        return argparse.Namespace(**{**vars(args), "workload": name, "steps": max(1, args.config_steps),
+                                     "warmup": 3, "no_e2e": True, "no_cpu_baseline": True})
+
+    def packed(line):
+        at, ro = line["kernels"]["attn_fwd"], line["kernels"]["rope"]
+        return {"workload": line["config"]["workload"], "segments": len(line["config"]["cu_seqlens"]) - 1,
+                "bound": "tensor", "attn_ms": at["ms"], "attn_ms_median": at["ms_median"],
+                "attn_tflops": at["tflops"], "frac": at["tflops"] / peaks["bf16_tflops"],
+                "frac_of_sustained": at["tflops"] / peaks["bf16_tflops_sustained"],
+                "frac_at_sampled_clock": line["roofline"]["frac_at_sampled_clock"],
+                "rope_ms": ro["ms"], "rope_frac_hbm": ro["frac_hbm"],
+                "sm_mhz_loaded": line["clocks"].get("sm_mhz_loaded")}
+
+    out = {"steps_each": max(1, args.config_steps), "warmup_each": 3,
+           "peaks": {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"],
+                     "source": peaks["source"]}}
+    t0 = time.time()
+    out["single_request_4k"] = packed(run_packed(sub("single_request_4k"), rank, world, dev, h3, peaks))
+    torch.cuda.empty_cache()
+    wl = workloads.continuation_batch()
+    out["continuation_batch"] = packed(run_packed(sub("continuation_batch"), rank, world, dev, h3, peaks, wl))
+    torch.cuda.empty_cache()
+    wl.cu_seqlens = np.asarray(wl.cu_requests, dtype=np.int32)  # one segment per request
+    wl.name = "continuation_4req_4seg_40x128"
+    out["continuation_batch_4seg"] = packed(run_packed(sub("continuation_batch_4seg"), rank, world, dev, h3,
+                                                       peaks, wl))
+    del wl
+    torch.cuda.empty_cache()
+
+    w = run_window(sub("window_grid"), rank, world, dev, h3, peaks)
+    out["window_grid"] = {"workload": w["config"]["workload"], "bound": "hbm",
+                          "in_place_roofline": w["roofline"], "layers": w["layers"],
+                          "in_place_ms_per_layer_pair": w["ms_per_step"],
+                          "packed_ms_per_layer_pair": w["packed_path"]["ms_per_step"]}
+    torch.cuda.empty_cache()
+    vs = run_vsa(sub("vsa_video"), rank, world, dev, h3, peaks)
+    ka = vs["kernels"]["attn"]
+    out["vsa_video"] = {"workload": vs["config"]["workload"], "bound": "tensor",
+                        "select_ms": vs["kernels"]["select"]["ms"], "attn_ms": ka["ms"],
+                        "tflops_useful": ka["tflops_useful"], "frac_useful": ka["tflops_useful"] / peaks["bf16_tflops"],
+                        "tflops_executed": ka["tflops_executed"],
+                        "frac_executed": ka["tflops_executed"] / peaks["bf16_tflops"],
+                        "executed_over_useful": ka["tflops_executed"] / ka["tflops_useful"],
+                        "shared_selection_frac": ka["shared_selection_frac"], "steps": ka["steps"],
+                        "steps_unshared": ka["steps_unshared"]}
+    torch.cuda.empty_cache()
+    cw = run_continuation(sub("continuation_window"), rank, world, dev, h3, peaks)
+    out["continuation_window"] = {"workload": cw["config"]["workload"], "bound": "hbm",
+                                  **{k: {"ms": v["ms"], "gbs": v["gbs"], "frac_hbm": v["frac_hbm"]}
+                                     for k, v in cw["kernels"].items()}}
+    torch.cuda.empty_cache()
+    lat = run_latency(sub("tiny_example"), rank, world, dev, h3)
+    out["tiny_example"] = {"workload": lat["config"]["workload"], "bound": "launch latency",
+                           **lat["latency_us"]}
+    out["wall_s"] = time.time() - t0
+    return out
 
 
 def run_e2e(args, world, dev, h3, wl, q, k, v, pos, tag, cu, cu_req, frames, flops, max_seqlen, ws):
@@ -628,20 +738,19 @@ def run_window(args, rank, world, dev, h3, peaks):
                 "frac": achieved / peaks["hbm_gbs"], "traffic": None,
                 "peak_source": "%s (copy bandwidth)" % peaks["source"],
                 "kernel": "attn_fwd_kernel<%d, window>" % D}
-    if rank == 0:
-        value = job_throughput(sum(flops), world, fused_ms_per_step)
-        print(json.dumps({
-            "metric": "shifted 3D window attention TFLOP/s (2 layers, attention in place on the grid)",
-            "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": max(3, args.warmup), "ms_per_step": fused_ms_per_step, "higher_is_better": True,
-            "packed_path": {"ms_per_step": ms_per_step,
-                            "value": job_throughput(sum(flops), world, ms_per_step),
-                            "note": "window pack -> varlen attention -> unpack per layer"},
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.name, "tokens": n, "heads": H, "head_dim": D,
-                       "l2": "inputs larger than L2 (%d MB per tensor)" % round(n * row / 1e6)},
-            "layers": per, "roofline": roofline, "clocks": clocks,
-            "gpu_launches": 2 * args.steps}), flush=True)
+    value = job_throughput(sum(flops), world, fused_ms_per_step)
+    return {
+        "metric": "shifted 3D window attention TFLOP/s (2 layers, attention in place on the grid)",
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": fused_ms_per_step, "higher_is_better": True,
+        "packed_path": {"ms_per_step": ms_per_step,
+                        "value": job_throughput(sum(flops), world, ms_per_step),
+                        "note": "window pack -> varlen attention -> unpack per layer"},
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "tokens": n, "heads": H, "head_dim": D,
+                   "l2": "inputs larger than L2 (%d MB per tensor)" % round(n * row / 1e6)},
+        "layers": per, "roofline": roofline, "clocks": clocks,
+        "gpu_launches": 2 * args.steps}
 
 
 def run_vsa(args, rank, world, dev, h3, peaks):
@@ -717,32 +826,31 @@ def run_vsa(args, rank, world, dev, h3, peaks):
     sel_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     attn_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
     attn_tflops = flops / attn_ms / 1e9
-    if rank == 0:
-        print(json.dumps({
-            "metric": ("block-sparse video attention TFLOP/s (attention over a fixed selection: paired "
-                       "query blocks share half their blocks)" if fixed_sel else
-                       "block-sparse video attention TFLOP/s (gate + top-k + attention over selected blocks)"),
-            "value": job_throughput(flops, world, ms_per_step), "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": {"workload": wl.name, "tokens": n, "heads": H, "head_dim": D, "blocks": nblk,
-                       "topk": wl.topk, "attention_flop_useful": flops,
-                       "l2": "inputs larger than L2 (%d MB per tensor)" % round(n * H * D * 2 / 1e6)},
-            "kernels": {"select": {"ms": sel_ms, "note": "block means + fp32 score GEMM + radix top-k"},
-                        "attn": {"ms": attn_ms, "tflops_useful": attn_tflops,
-                                 "tflops_executed": flops_executed / attn_ms / 1e9,
-                                 "shared_selection_frac": float(shared.mean() / wl.topk),
-                                 "steps": int(steps.sum()), "steps_unshared": int(steps.size * wl.topk),
-                                 "note": "each 128-row tile holds two query blocks; a step stacks two "
-                                         "key blocks, and a block selected by only one of them is "
-                                         "masked for the other half"}},
-            "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": attn_tflops / peaks["bf16_tflops"], "traffic": None,
-                         "kernel": "attn_fwd_kernel<%d, vsa>" % D,
-                         "peak_source": peaks["source"] + " bf16_tflops (burst)",
-                         "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"]},
-            "clocks": clocks, "gpu_launches": (2 if fixed_sel else 5) * args.steps}), flush=True)
+    return {
+        "metric": ("block-sparse video attention TFLOP/s (attention over a fixed selection: paired "
+                   "query blocks share half their blocks)" if fixed_sel else
+                   "block-sparse video attention TFLOP/s (gate + top-k + attention over selected blocks)"),
+        "value": job_throughput(flops, world, ms_per_step), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "tokens": n, "heads": H, "head_dim": D, "blocks": nblk,
+                   "topk": wl.topk, "attention_flop_useful": flops,
+                   "l2": "inputs larger than L2 (%d MB per tensor)" % round(n * H * D * 2 / 1e6)},
+        "kernels": {"select": {"ms": sel_ms, "note": "block means + fp32 score GEMM + radix top-k"},
+                    "attn": {"ms": attn_ms, "tflops_useful": attn_tflops,
+                             "tflops_executed": flops_executed / attn_ms / 1e9,
+                             "shared_selection_frac": float(shared.mean() / wl.topk),
+                             "steps": int(steps.sum()), "steps_unshared": int(steps.size * wl.topk),
+                             "note": "each 128-row tile holds two query blocks; a step stacks two "
+                                     "key blocks, and a block selected by only one of them is "
+                                     "masked for the other half"}},
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": attn_tflops / peaks["bf16_tflops"], "traffic": None,
+                     "kernel": "attn_fwd_kernel<%d, vsa>" % D,
+                     "peak_source": peaks["source"] + " bf16_tflops (burst)",
+                     "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"]},
+        "clocks": clocks, "gpu_launches": (2 if fixed_sel else 5) * args.steps}
 
 
 def run_continuation(args, rank, world, dev, h3, peaks):
@@ -812,22 +920,21 @@ def run_continuation(args, rank, world, dev, h3, peaks):
         t = float(np.mean([e[a].elapsed_time(e[b]) for e in evs]))
         per[name] = {"ms": t, "bytes": nbytes, "gbs": nbytes / t / 1e6, "frac_hbm": nbytes / t / 1e6 / peaks["hbm_gbs"]}
     total_bytes = pack_bytes + upd_bytes + app_bytes
-    if rank == 0:
-        achieved = per["pack"]["gbs"]
-        print(json.dumps({
-            "metric": "continuation window GB/s (pack + target-only update + append)",
-            "value": world * total_bytes / ms / 1e6, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "continuation_h3_window_29x40x50_a200", "packed_rows": n,
-                       "row_bytes": row_bytes, "start_frame": plan.start_frame, "audio_cut": plan.audio_cut,
-                       "l2": "inputs larger than L2 (%.0f MB packed)" % (n * row_bytes / 1e6)},
-            "kernels": per,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-                         "kernel": "continuation_pack_kernel",
-                         "peak_source": "%s (copy bandwidth)" % peaks["source"]},
-            "clocks": clocks, "gpu_launches": 3 * args.steps}), flush=True)
+    achieved = per["pack"]["gbs"]
+    return {
+        "metric": "continuation window GB/s (pack + target-only update + append)",
+        "value": world * total_bytes / ms / 1e6, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "continuation_h3_window_29x40x50_a200", "packed_rows": n,
+                   "row_bytes": row_bytes, "start_frame": plan.start_frame, "audio_cut": plan.audio_cut,
+                   "l2": "inputs larger than L2 (%.0f MB packed)" % (n * row_bytes / 1e6)},
+        "kernels": per,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "continuation_pack_kernel",
+                     "peak_source": "%s (copy bandwidth)" % peaks["source"]},
+        "clocks": clocks, "gpu_launches": 3 * args.steps}
 
 
 def run_latency(args, rank, world, dev, h3):
@@ -876,16 +983,15 @@ def run_latency(args, rank, world, dev, h3):
     eager_us, graph_us = timed(step), timed(graph.replay)
     if h3.get_device_error(dev) != 0:
         raise RuntimeError("device error during the timed steps")
-    if rank == 0:
-        print(json.dumps({
-            "metric": "worked-example step latency (RoPE + varlen attention, 45 tokens)",
-            "value": graph_us, "unit": "us", "n_gpus": world, "steps": reps, "warmup": max(3, args.warmup),
-            "ms_per_step": graph_us / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.name, "tokens": N, "cu_seqlens": [int(x) for x in wl.cu_seqlens],
-                       "heads": H, "head_dim": D},
-            "latency_us": {"cuda_graph_replay": graph_us, "eager": eager_us},
-            "gpu_launches": 3 * reps}), flush=True)
+    return {
+        "metric": "worked-example step latency (RoPE + varlen attention, 45 tokens)",
+        "value": graph_us, "unit": "us", "n_gpus": world, "steps": reps, "warmup": max(3, args.warmup),
+        "ms_per_step": graph_us / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "tokens": N, "cu_seqlens": [int(x) for x in wl.cu_seqlens],
+                   "heads": H, "head_dim": D},
+        "latency_us": {"cuda_graph_replay": graph_us, "eager": eager_us},
+        "gpu_launches": 3 * reps}
 
 
 def _block_sizes(grid, block):

@@ -425,6 +425,25 @@ H3_API h3_status h3_sp_exchange_plan(const int32_t grid[3], const int32_t win[3]
                                      int32_t* send_index, int64_t* recv_counts,
                                      int32_t* recv_position);
 
+/* ---- Testing hooks of the timeout path (no page counterpart) --------------------------------
+ * Every wait between the warps of an attention kernel (h3_varlen_attn_fwd, its no-alloc form,
+ * h3_window_attn_fwd, h3_vsa_attn_fwd) is bounded.  A wait that runs out records H3_ERR_TIMEOUT;
+ * the kernel then waits (always with the default 2 s limit) for the copies and matrix products it
+ * has already issued, releases its tensor memory and returns, and every later attention launch
+ * leaves at once until h3_get_device_error() clears the error.  Outputs of a launch that timed
+ * out are unspecified (partly written).  These two process-wide settings let tests drive that
+ * path; they apply to attention launches issued after the call. */
+
+/* Limit, in nanoseconds, of the pipeline waits; 0 restores the default of 2 s.  Returns the limit
+ * in force before the call. */
+H3_API uint64_t h3_set_wait_limit_ns(uint64_t nanoseconds);
+
+/* The key/value loader of each attention CTA issues at most `tiles` tiles and then stops, as if
+ * it had stalled, so the waits of the warps that consume them run out; negative (the default)
+ * restores normal operation.  Nothing is read or written out of bounds and every wait still ends
+ * by its limit.  Returns the previous setting. */
+H3_API int32_t h3_debug_stall_loads(int32_t tiles);
+
 /* Synchronises `stream`, returns the first device-side error recorded on the current device
  * since the last call (H3_OK if none) and clears it. */
 H3_API h3_status h3_get_device_error(h3_stream_t stream);

@@ -124,6 +124,8 @@ def load_library():
         "h3_vsa_select": (I32, [P, P, I32P, I32P, I32, I32, I32, F32, P, P, P, U64, P]),
         "h3_vsa_attn_workspace_size": (U64, [I32P, I32P, I32, I32]),
         "h3_vsa_attn_fwd": (I32, [P, P, P, P, P, I32P, I32P, I32, I32, P, I32, F32, P, U64, P]),
+        "h3_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
+        "h3_debug_stall_loads": (I32, [I32]),
         "h3_get_device_error": (I32, [P]),
         "h3_status_string": (ctypes.c_char_p, [I32]),
         "h3_version": (I32, []),
@@ -646,3 +648,15 @@ def get_device_error(device: Optional[torch.device] = None) -> int:
     lib = load_library()
     with torch.cuda.device(dev):
         return int(lib.h3_get_device_error(_stream(dev)))
+
+
+def set_wait_limit_ns(nanoseconds: int) -> int:
+    """Limit of the attention kernels' internal waits for later launches (0 = the 2 s default);
+    returns the previous limit.  A testing hook for the timeout path: see h3_set_wait_limit_ns."""
+    return int(load_library().h3_set_wait_limit_ns(int(nanoseconds)))
+
+
+def debug_stall_loads(tiles: int) -> int:
+    """Make each attention CTA's key/value loader stop after `tiles` tiles (negative = never);
+    returns the previous setting.  A testing hook for the timeout path: see h3_debug_stall_loads."""
+    return int(load_library().h3_debug_stall_loads(int(tiles)))

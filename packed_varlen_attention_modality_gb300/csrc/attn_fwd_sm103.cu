@@ -84,6 +84,8 @@ constexpr int kSortMax = 256;         // segments ordered longest-first up to th
 constexpr int kWsHeader = kAttnWsHeaderWords;  // workspace words: (spare), total items, 2 spare
 constexpr int kPersistMaxSeqlen = 2048;  // loop over items per CTA up to this segment length
 
+static_assert(kDefaultWaitLimitNs == kWaitLimitNs, "host and device default wait limits agree");
+
 constexpr int kModePacked = kAttnModePacked;  // kernel variants (see h3_internal.h)
 constexpr int kModeWindow = kAttnModeWindow;
 constexpr int kModeVsa = kAttnModeVsa;
@@ -401,7 +403,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 int capacity, int num_heads, float scale, float scale_log2,
                 uint32_t* __restrict__ ws, const __grid_constant__ WindowAttnGeom wg,
                 const uint2* __restrict__ vsa_steps, const int2* __restrict__ vsa_counts,
-                unsigned int* err) {
+                unsigned int* err, unsigned long long wait_ns, unsigned int stall_after) {
   constexpr bool kWin = kMode == kModeWindow;
   constexpr bool kVsa = kMode == kModeVsa;
   using C = Cfg<D, kMode>;
@@ -436,6 +438,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Waits of the pipeline give up after wait_ns (2 s unless a test shortens it); the drains at
+  // the end always allow the full 2 s, since what they wait for (copies and MMAs already issued)
+  // completes by itself.
+  auto pwait = [&](uint32_t bar, uint32_t parity) { return mbar_wait(bar, parity, wait_ns); };
+  // Testing hook: a producer stops issuing key/value loads once it has issued stall_after tiles
+  // (never, by default), as if it had stalled; the waits of the roles that consume them then run
+  // out and the kernel unwinds.  Every wait still ends (by its limit) and no access changes.
+  bool stalled = false;
 
   // A wait that timed out earlier (recorded, not yet read) means the machinery is not healthy:
   // leave at once instead of running into 2-second waits again.
@@ -504,8 +514,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (t >= nt || j >= d.nkv_t[t]) continue;
+        if (cnt >= stall_after) {
+          stalled = true;
+          return true;
+        }
         const uint32_t s = cnt % S;
-        if (!mbar_wait(empty0 + 8 * s, ((cnt / S) & 1) ^ 1)) return false;
+        if (!pwait(empty0 + 8 * s, ((cnt / S) & 1) ^ 1)) return false;
         mbar_arrive_expect_tx(full0 + 8 * s, C::kTileBytes);
         vsa_load_tile<C::kBoxes, C::kBoxBytes>(ring + s * C::kTileBytes, map, d.head,
                                                static_cast<int>(cur[t].x & kVsaBlockMask),
@@ -550,7 +564,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
             d.head = 0;
             d.q0 = 0;
           }
-          ok = mbar_wait(bar_wempty(k & 1), ((k >> 1) & 1) ^ 1);
+          ok = pwait(bar_wempty(k & 1), ((k >> 1) & 1) ^ 1);
           if (!ok) break;
           work[k & 1] = d;
           mbar_arrive(bar_wfull(k & 1));
@@ -572,7 +586,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
             }
           };
           // Q tiles: after the previous item's last QK^T has read the buffers
-          ok = mbar_wait(bar_qempty, (k & 1) ^ 1);
+          ok = pwait(bar_qempty, (k & 1) ^ 1);
           if (!ok) break;
           if constexpr (kVsa) {
             int qb[2][2];
@@ -587,6 +601,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
             }
             ok = vsa_stream(d, std::integral_constant<int, SK>{}, sK, &tmap_k, bar_kfull(0),
                             bar_kempty(0), kt);
+            if (stalled) break;
           } else {
             for (int t = 0; t < (has1 ? 2 : 1); ++t) {
               mbar_arrive_expect_tx(bar_qfull(t), C::kTileBytes);
@@ -594,20 +609,25 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
               ++qn[t];
             }
             for (int j = 0; j < nkv && ok; ++j) {
+              if (kt >= stall_after) {
+                stalled = true;
+                break;
+              }
               const int row = d.seg_start + j * kBlockN;
               const int s = static_cast<int>(kt % SK);
-              ok = mbar_wait(bar_kempty(s), ((kt / SK) & 1) ^ 1);
+              ok = pwait(bar_kempty(s), ((kt / SK) & 1) ^ 1);
               if (!ok) break;
               mbar_arrive_expect_tx(bar_kfull(s), C::kTileBytes);
               load_tile(sK + s * C::kTileBytes, hhalf ? &tmap_k2 : &tmap_k, j, row, bar_kfull(s));
               ++kt;
               const int v = static_cast<int>(vt % SV);
-              ok = mbar_wait(bar_vempty(v), ((vt / SV) & 1) ^ 1);
+              ok = pwait(bar_vempty(v), ((vt / SV) & 1) ^ 1);
               if (!ok) break;
               mbar_arrive_expect_tx(bar_vfull(v), C::kTileBytes);
               load_tile(sV + v * C::kTileBytes, hhalf ? &tmap_v2 : &tmap_v, j, row, bar_vfull(v));
               ++vt;
             }
+            if (stalled) break;
           }
         }
         if (!ok) record_error(err, kErrTimeout);
@@ -629,7 +649,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       // ================= MMA issuer =================
       // every lane waits and the verdict is made warp-uniform, so the warp never diverges
       auto wait_all = [&](uint32_t bar, uint32_t parity) {
-        return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+        return __all_sync(0xffffffffu, pwait(bar, parity));
       };
       // Two barriers at once: the first polls are issued back to back so their latencies (about
       // 100-200 cycles each, even on a completed phase) overlap instead of adding up.  Used where
@@ -639,8 +659,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       auto wait_all2 = [&](uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1) {
         bool r0 = mbar_try_wait(b0, p0);
         bool r1 = mbar_try_wait(b1, p1);
-        if (!r0) r0 = mbar_wait(b0, p0);
-        if (!r1) r1 = mbar_wait(b1, p1);
+        if (!r0) r0 = pwait(b0, p0);
+        if (!r1) r1 = pwait(b1, p1);
         return __all_sync(0xffffffffu, r0 && r1);
       };
 
@@ -844,13 +864,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         uint32_t vt = 0;  // V tiles loaded so far
         bool ok = true;
         for (int k = 0; ok; ++k) {
-          ok = mbar_wait(bar_wfull(k & 1), (k >> 1) & 1);
+          ok = pwait(bar_wfull(k & 1), (k >> 1) & 1);
           if (!ok) break;
           const WorkDesc d = work[k & 1];
           mbar_arrive(bar_wempty(k & 1));
           if (d.seg_len < 0) break;
           ok = vsa_stream(d, std::integral_constant<int, SV>{}, sV, &tmap_v, bar_vfull(0),
                           bar_vempty(0), vt);
+          if (stalled) break;
         }
         if (!ok) record_error(err, kErrTimeout);
         for (uint32_t i = 0; i < SV && i < vt; ++i) {  // drain, as for the other producer
@@ -874,7 +895,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     uint32_t sn = 0, fn = 0;  // S groups and final-O completions seen by this tile slot
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_wfull(k & 1), (k >> 1) & 1));
+      ok = __all_sync(0xffffffffu, pwait(bar_wfull(k & 1), (k >> 1) & 1));
       if (!ok) break;
       const WorkDesc d = work[k & 1];
       __syncwarp();
@@ -947,7 +968,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
             vkm1 = vsa_block_mask(static_cast<int>(e.y & kVsaBlockMask), wg);
           }
         }
-        ok = mbar_wait(bar_sfull(t), sn++ & 1);
+        ok = pwait(bar_sfull(t), sn++ & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         if constexpr (kVsa) {
@@ -1078,7 +1099,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16 rows of this segment; LSE; then O_t is free again ----
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_ofinal(t), fn++ & 1));
+      ok = __all_sync(0xffffffffu, pwait(bar_ofinal(t), fn++ & 1));
       if (!ok) break;
       tc_fence_after();
       int q_row;  // this thread's row in the output (original row-major order for windows)
@@ -1206,7 +1227,7 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
       a.tmap_q, a.tmap_k, a.tmap_v, half ? a.tmap_q2 : a.tmap_q, half ? a.tmap_k2 : a.tmap_k,
       half ? a.tmap_v2 : a.tmap_v, static_cast<__nv_bfloat16*>(a.o), a.lse, a.cu_seqlens,
       a.num_segments, a.capacity, a.num_heads, a.scale, scale_log2, ws, a.wg, a.vsa_steps,
-      a.vsa_counts, a.err);
+      a.vsa_counts, a.err, static_cast<unsigned long long>(a.wait_limit_ns), a.stall_after_tiles);
   return cudaGetLastError();
 }
 

@@ -90,7 +90,17 @@ struct AttnArgs {
   float scale;
   void* workspace;  // attn_workspace_bytes(num_segments) bytes: the work plan
   unsigned int* err;
+  uint64_t wait_limit_ns;  // limit of the kernel's pipeline waits (wait_limit_ns() below)
+  uint32_t stall_after_tiles;  // testing hook: producers stop after this many K/V tiles
 };
+
+// Limit of the attention kernels' pipeline waits for launches from now on: 2 s unless
+// h3_set_wait_limit_ns changed it.
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
+uint64_t wait_limit_ns();
+// Key/value tiles a producer of an attention CTA issues before it stops (all, unless
+// h3_debug_stall_loads changed it).
+uint32_t stall_after_tiles();
 
 // Workspace of the packed variant (uint32 words): [1] total items, [kAttnWsHeaderWords, +S)
 // segment order, [kAttnWsHeaderWords + S, +S+1) exclusive prefix of items in that order; the

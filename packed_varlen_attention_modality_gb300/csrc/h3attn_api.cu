@@ -4,6 +4,7 @@
 // error word below (a static __device__ variable, 4 bytes per device), where kernels record the
 // first device-side problem they meet (bad cu_seqlens, bad permutation entry, a timed-out wait).
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -134,11 +135,35 @@ void* noalloc_scratch_ptr() {
   return g_noalloc_ptr[dev];
 }
 
+std::atomic<uint64_t> g_wait_limit_ns{0};  // 0: the default
+std::atomic<int32_t> g_stall_after{-1};    // negative: never
+
 }  // namespace
+
+namespace h3 {
+uint64_t wait_limit_ns() {
+  const uint64_t v = g_wait_limit_ns.load(std::memory_order_relaxed);
+  return v == 0 ? kDefaultWaitLimitNs : v;
+}
+uint32_t stall_after_tiles() {
+  const int32_t v = g_stall_after.load(std::memory_order_relaxed);
+  return v < 0 ? 0xffffffffu : static_cast<uint32_t>(v);
+}
+}  // namespace h3
 
 extern "C" {
 
 int32_t h3_version(void) { return 100; }
+
+uint64_t h3_set_wait_limit_ns(uint64_t nanoseconds) {
+  const uint64_t prev = h3::wait_limit_ns();
+  g_wait_limit_ns.store(nanoseconds, std::memory_order_relaxed);
+  return prev;
+}
+
+int32_t h3_debug_stall_loads(int32_t tiles) {
+  return g_stall_after.exchange(tiles < 0 ? -1 : tiles, std::memory_order_relaxed);
+}
 
 const char* h3_status_string(h3_status s) {
   switch (s) {
@@ -272,6 +297,8 @@ h3_status h3_varlen_attn_fwd(const void* q, const void* k, const void* v, void* 
   a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(head_dim));
   a.workspace = workspace;
   a.err = device_error_ptr();
+  a.wait_limit_ns = h3::wait_limit_ns();
+  a.stall_after_tiles = h3::stall_after_tiles();
   if (a.err == nullptr) return H3_ERR_CUDA;
   return from_cuda(h3::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -318,6 +345,8 @@ h3_status h3_varlen_attn_fwd_noalloc(const void* q, const void* k, const void* v
   a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(head_dim));
   a.workspace = scratch;  // the plan kernel rewrites every word the attention kernel reads
   a.err = device_error_ptr();
+  a.wait_limit_ns = h3::wait_limit_ns();
+  a.stall_after_tiles = h3::stall_after_tiles();
   if (a.err == nullptr) return H3_ERR_CUDA;
   return from_cuda(h3::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -376,6 +405,8 @@ h3_status h3_window_attn_fwd(const void* q, const void* k, const void* v, void* 
   a.head_dim = head_dim;
   a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(head_dim));
   a.err = device_error_ptr();
+  a.wait_limit_ns = h3::wait_limit_ns();
+  a.stall_after_tiles = h3::stall_after_tiles();
   if (a.err == nullptr) return H3_ERR_CUDA;
   return from_cuda(h3::launch_attn_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -622,6 +653,8 @@ h3_status h3_vsa_attn_fwd(const void* q, const void* k, const void* v, void* o, 
   a.head_dim = head_dim;
   a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(head_dim));
   a.err = err;
+  a.wait_limit_ns = h3::wait_limit_ns();
+  a.stall_after_tiles = h3::stall_after_tiles();
   // the pairs' key/value schedule, then the attention that follows it (same stream)
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t ce = h3::launch_vsa_schedule(block_idx, static_cast<int>(nblk), num_heads,

@@ -56,6 +56,21 @@ def test_workspace_size_grows_with_segments(lib):
     assert sizes[-1] >= 8 * 65535 and lib.h3_varlen_attn_workspace_size(0, 40, 1, 128) == 0
 
 
+def test_wait_limit_setting_returns_the_previous_and_zero_restores_the_default(lib):
+    default = 2_000_000_000
+    assert lib.h3_set_wait_limit_ns(0) == default
+    assert lib.h3_set_wait_limit_ns(1500) == default
+    assert lib.h3_set_wait_limit_ns(0) == 1500
+    assert lib.h3_set_wait_limit_ns(0) == default
+
+
+def test_stall_setting_returns_the_previous(lib):
+    assert lib.h3_debug_stall_loads(-1) == -1
+    assert lib.h3_debug_stall_loads(3) == -1
+    assert lib.h3_debug_stall_loads(-5) == 3
+    assert lib.h3_debug_stall_loads(-1) == -1
+
+
 def test_version_and_status_strings(lib):
     assert lib.h3_version() == 100
     for s in range(11):
