@@ -545,6 +545,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           total = static_cast<uint32_t>((vsa_num_blocks(wg) + 3) / 4 * num_heads);
         else
           total = ws[1];
+        const uint64_t pol_keep = l2_policy_evict_last(), pol_stream = l2_policy_evict_first();
         uint32_t kt = 0, vt = 0;  // K / V tiles loaded so far (positions in the rings)
         uint32_t qn[2] = {0u, 0u};  // Q tiles loaded so far, per tile slot
         bool ok = true;
@@ -575,14 +576,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           // tile loads: packed rows [row, row + 128) of one head; window box (w, h, t) of frames,
           // from the half-height map for a half edge window
           const bool hhalf = kWin && d.hbox != wg.w[1];
+          // packed segments: every CTA of a (segment, head) streams the same key/value tiles, so
+          // they are kept in L2 in preference to the query tiles, which are read once
           auto load_tile = [&](uint8_t* dst, const CUtensorMap* map, int tile, int row,
-                               uint32_t bar) {
+                               uint32_t bar, uint64_t policy) {
             for (int b = 0; b < C::kBoxes; ++b) {
               if constexpr (kWin)
                 tma_load_5d(smem_u32(dst + b * C::kBoxBytes), map, b * 64, d.head, d.box[2],
                             d.box[1], d.box[0] + tile * d.fpt, bar);
               else
-                tma_load_3d(smem_u32(dst + b * C::kBoxBytes), map, b * 64, d.head, row, bar);
+                tma_load_3d_hint(smem_u32(dst + b * C::kBoxBytes), map, b * 64, d.head, row, bar,
+                                 policy);
             }
           };
           // Q tiles: after the previous item's last QK^T has read the buffers
@@ -605,7 +609,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
           } else {
             for (int t = 0; t < (has1 ? 2 : 1); ++t) {
               mbar_arrive_expect_tx(bar_qfull(t), C::kTileBytes);
-              load_tile(sQ + t * C::kTileBytes, hhalf ? &tmap_q2 : &tmap_q, t, d.q0 + t * kBlockM, bar_qfull(t));
+              load_tile(sQ + t * C::kTileBytes, hhalf ? &tmap_q2 : &tmap_q, t, d.q0 + t * kBlockM,
+                        bar_qfull(t), pol_stream);
               ++qn[t];
             }
             for (int j = 0; j < nkv && ok; ++j) {
@@ -618,13 +623,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
               ok = pwait(bar_kempty(s), ((kt / SK) & 1) ^ 1);
               if (!ok) break;
               mbar_arrive_expect_tx(bar_kfull(s), C::kTileBytes);
-              load_tile(sK + s * C::kTileBytes, hhalf ? &tmap_k2 : &tmap_k, j, row, bar_kfull(s));
+              load_tile(sK + s * C::kTileBytes, hhalf ? &tmap_k2 : &tmap_k, j, row, bar_kfull(s),
+                        pol_keep);
               ++kt;
               const int v = static_cast<int>(vt % SV);
               ok = pwait(bar_vempty(v), ((vt / SV) & 1) ^ 1);
               if (!ok) break;
               mbar_arrive_expect_tx(bar_vfull(v), C::kTileBytes);
-              load_tile(sV + v * C::kTileBytes, hhalf ? &tmap_v2 : &tmap_v, j, row, bar_vfull(v));
+              load_tile(sV + v * C::kTileBytes, hhalf ? &tmap_v2 : &tmap_v, j, row, bar_vfull(v),
+                        pol_keep);
               ++vt;
             }
             if (stalled) break;
@@ -889,6 +896,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const uint32_t s_addr = tmem + lane_base + kColS + 128 * t;
     const uint32_t o_addr = tmem + lane_base + kColO + 128 * t;
     const float2 c2 = make_float2(scale_log2, scale_log2);
+    const uint64_t pol_out = l2_policy_evict_first();
     bool vsa_partial = false;  // VSA: some blocks are cropped by the grid edge (keys need masks)
     if constexpr (kVsa)
       vsa_partial = (wg.L[0] % wg.w[0]) != 0 || (wg.L[1] % wg.w[1]) != 0 || (wg.L[2] % wg.w[2]) != 0;
@@ -1146,8 +1154,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          for (int c = 0; c < 4; ++c) {
+            const uint4 val = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            if constexpr (kMode == kModePacked)
+              st_global_v4_hint(dst + c, val, pol_out);  // written once: not kept over K/V
+            else
+              dst[c] = val;
+          }
         }
       }
       tc_fence_before();
