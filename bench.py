@@ -480,7 +480,9 @@ def run_packed(args, rank, world, dev, h3, peaks, wl=None):
                                  "ms_min": float(np.min(attn_each)),
                                  "tflops_median": flops / (float(np.median(attn_each)) / 1e3) / 1e12}},
         "clocks": clocks,
-        "gpu_launches": 3 * args.steps,   # RoPE, attention plan, attention per step
+        # RoPE, attention plan, attention per step, and the merge of split items when the workspace
+        # holds the split area (segments of 1,024 rows or more)
+        "gpu_launches": (4 if max_seqlen >= 1024 else 3) * args.steps,
         "e2e": e2e,
         "cpu_baseline": cpu,
     }

@@ -115,9 +115,14 @@ H3_API h3_status h3_rope_apply(const void* q_in, void* q_out, const void* k_in, 
                         const int32_t* cu_requests, int32_t num_requests,
                         const float* start_frames, const h3_rope_cfg* cfg, h3_stream_t stream);
 
-/* Bytes of device workspace h3_varlen_attn_fwd needs for these sizes: the work plan written by
- * the call itself (segment order and item prefix, 8 bytes per segment, plus a 16-byte header),
- * rounded up to 256.  0 when num_segments <= 0. */
+/* Bytes of device workspace h3_varlen_attn_fwd wants for these sizes: the work plan written by
+ * the call itself (segment order and item prefix, 8 bytes per segment, plus a 16-byte header,
+ * rounded up to 256) and, when max_seqlen >= 1024, a split area after it (about 42 MB at
+ * head_dim 128, 21 MB at 64).  With the split area the call may cut the long work items of its
+ * last, partly filled wave of CTAs into chunks of their key range, so that the wave spreads over
+ * every SM; the chunks' partial results are merged in a fixed order, so the output does not
+ * depend on which chunk finishes last.  The plan alone (the size returned for max_seqlen < 1024)
+ * is the minimum the call accepts; it then never splits.  0 when num_segments <= 0. */
 H3_API size_t h3_varlen_attn_workspace_size(int32_t num_segments, int32_t num_heads,
                                      int32_t max_seqlen, int32_t head_dim);
 
@@ -138,9 +143,9 @@ H3_API size_t h3_varlen_attn_workspace_size(int32_t num_segments, int32_t num_he
  *               full but reported as H3_ERR_BAD_CU_SEQLENS.
  * softmax_scale: <= 0 selects 1/sqrt(head_dim).
  * workspace   : device scratch of h3_varlen_attn_workspace_size() bytes (16-byte aligned), or
- *               NULL when that size is 0.  Contents need not be initialised; the call rewrites
- *               them.  Calls that may run at the same time (other streams) need separate
- *               workspaces.
+ *               NULL when that size is 0; at least the plan (see there).  Contents need not be
+ *               initialised; the call rewrites what it reads.  Calls that may run at the same
+ *               time (other streams) need separate workspaces.
  * Errors: H3_ERR_NULL, H3_ERR_INVALID_ARG, H3_ERR_UNSUPPORTED, H3_ERR_MISALIGNED,
  *         H3_ERR_WORKSPACE, H3_ERR_CUDA; device-side H3_ERR_BAD_CU_SEQLENS / H3_ERR_TIMEOUT.
  */
@@ -161,7 +166,9 @@ H3_API h3_status h3_varlen_attn_fwd(const void* q, const void* k, const void* v,
  *
  * Same inputs, outputs, semantics and errors as h3_varlen_attn_fwd.  Instead of a workspace it
  * uses a fixed array inside the library (132 KB per device, held from the first use until the
- * process exits), so it calls no cudaMalloc, cudaFree or other allocating routine.
+ * process exits), so it calls no cudaMalloc, cudaFree or other allocating routine.  The array
+ * holds the plan alone, so work items are never split: the result is, bit for bit, that of
+ * h3_varlen_attn_fwd given a plan-only workspace.
  *   - At most H3_NOALLOC_MAX_SEGMENTS segments; more returns H3_ERR_WORKSPACE, launching nothing.
  *   - The first call on each device looks up the array's device address (with that device
  *     current); make that first call before any stream capture.

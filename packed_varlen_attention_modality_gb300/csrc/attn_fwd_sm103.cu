@@ -83,6 +83,7 @@ constexpr int kPlanThreads = 1024;
 constexpr int kSortMax = 256;         // segments ordered longest-first up to this count
 constexpr int kWsHeader = kAttnWsHeaderWords;  // workspace words: (spare), total items, 2 spare
 constexpr int kPersistMaxSeqlen = 2048;  // loop over items per CTA up to this segment length
+constexpr int kPersistMaxWaves = 8;      // ... or when the job has at most this many waves of items
 
 static_assert(kDefaultWaitLimitNs == kWaitLimitNs, "host and device default wait limits agree");
 
@@ -91,6 +92,13 @@ constexpr int kModeWindow = kAttnModeWindow;
 constexpr int kModeVsa = kAttnModeVsa;
 constexpr int kVsaBlockRows = 64;  // rows of one VSA block = half a 128-row tile
 
+
+// Packed segments: the key/value tiles [kv0, kv0 + nkv) an item covers (all of its segment's,
+// unless the item is a chunk of a split one) and the split: (chunk << 16 | chunks), 0 for a
+// whole item; group = the split item's first entry in the split area.
+struct PackedChunk {
+  int kv0, split, group;
+};
 
 struct WorkDesc {
   int seg_start;  // packed: first row of the segment
@@ -104,7 +112,10 @@ struct WorkDesc {
   int nsh_t[2];   // VSA: key blocks both query blocks of the tile selected
   int hbox;       // window: box rows along H (the window's, or half of it for an edge window)
   int fpt;        // window: frames per 128-row tile (128 / (hbox * window W))
-  uint32_t mask[2][4];  // window: rows of each tile that lie inside the grid (= inside the window)
+  union {
+    uint32_t mask[2][4];  // window: rows of each tile that lie inside the grid (= inside the window)
+    PackedChunk pk;       // packed: the item's key range and split
+  };
 };
 
 struct ItemShape {
@@ -116,8 +127,11 @@ struct ItemShape {
 template <int kMode>
 __device__ __forceinline__ ItemShape shape_of(const WorkDesc& d) {
   if (kMode != kModePacked) return ItemShape{d.ntiles == 2, d.nkv, kBlockN};
-  const int nkv = (d.seg_len + kBlockN - 1) / kBlockN;
-  return ItemShape{d.q0 + kBlockM < d.seg_start + d.seg_len, nkv, d.seg_len - (nkv - 1) * kBlockN};
+  // a chunk of a split item covers key tiles [kv0, kv0 + nkv); only the segment's last key tile
+  // can be partial
+  const int nkv_seg = (d.seg_len + kBlockN - 1) / kBlockN;
+  const int last = d.pk.kv0 + d.nkv == nkv_seg ? d.seg_len - (nkv_seg - 1) * kBlockN : kBlockN;
+  return ItemShape{d.q0 + kBlockM < d.seg_start + d.seg_len, d.nkv, last};
 }
 
 // 128-bit row masks as (lo, hi) 64-bit halves.
@@ -258,11 +272,159 @@ __device__ __forceinline__ uint32_t items_of(int len, int heads) {
   return static_cast<uint32_t>((len + kRowsPerItem - 1) / kRowsPerItem) * heads;
 }
 
+// ---- Split of the last wave (packed segments) -------------------------------------------------
+// With G CTAs working at a time, items [F*G, T) of T whole items (F = T / G) form a last wave that
+// leaves most SMs idle when items are long (the 4,096-token request: 336 equal video items on 152
+// SMs).  The plan cuts each long item of that wave into chunks of its key tiles so that the wave's
+// work spreads over all G CTAs.  Each chunk writes its partial result (O normalised by its own row
+// sum, fp32, and its LSE) to the split area; a merge kernel then combines the chunks of every split
+// item in chunk order (so the result does not depend on which chunk finished first):
+//   lse = log sum_c exp(lse_c),   o = sum_c exp(lse_c - lse) o_c.
+// Split area (after the plan, 256-byte aligned): kSplitMaxEntries entries of 8 words, the list of
+// split items (their first entries; plan word 0 counts them), then per entry and query tile 128
+// rows of D fp32 values followed by their 128 fp32 LSEs.
+constexpr int kSplitMinTiles = 8;   // split only items of at least 8 key tiles (1,024 keys)
+constexpr int kSplitMaxChunks = 8;
+constexpr int kSplitMaxWave = 256;  // the split is planned for grids of at most this many CTAs
+struct SplitEntry {
+  int seg_start, seg_len, head, q0, kv0, kv1, group, split;  // split = chunk << 16 | chunks
+};
+static_assert(sizeof(SplitEntry) == 8 * sizeof(int32_t), "split entries are 8 words");
+__host__ __device__ constexpr size_t split_groups_offset() {  // first entries of the split items
+  return static_cast<size_t>(kSplitMaxEntries) * sizeof(SplitEntry);
+}
+__host__ __device__ constexpr size_t split_partials_offset() {
+  return split_groups_offset() + static_cast<size_t>(kSplitMaxEntries) * sizeof(uint32_t);
+}
+static_assert(split_partials_offset() % 16 == 0, "partial rows are written as 16-byte vectors");
+static_assert(split_partials_offset() + static_cast<size_t>(kSplitMaxEntries) * 2 * kBlockM * 129 *
+                      sizeof(float) == attn_split_bytes(128),
+              "split area layout agrees with its size");
+
+// Merge of split items.  Work unit (group, t, z): rows [16 z, 16 z + 16) of query tile t of the
+// split item whose first entry is the group's; the CTAs of a small fixed grid take the units in
+// turn.  Chunks are combined in chunk order.  Memory-bound and short: the partials were written
+// moments before and are read back from L2; every chunk's loads of a unit are issued together.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeRows = 16;  // rows per unit: 16 rows x D / 8 column groups = 256 threads at D = 128
+constexpr int kMergeUnitsPerGroup = 2 * (kBlockM / kMergeRows);
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads)
+attn_merge_kernel(const uint32_t* __restrict__ ws, const uint8_t* __restrict__ split_area,
+                  __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int num_heads,
+                  int capacity) {
+  __shared__ float s_w[kMergeRows][kSplitMaxChunks];  // per row: chunk weights exp(lse_c - lse)
+  __shared__ float s_lse[kMergeRows];
+  const int n_units = static_cast<int>(ws[0]) * kMergeUnitsPerGroup;
+  const uint32_t* groups = reinterpret_cast<const uint32_t*>(split_area + split_groups_offset());
+  constexpr size_t kSlot = static_cast<size_t>(kBlockM) * (D + 1);
+  const float* parts = reinterpret_cast<const float*>(split_area + split_partials_offset());
+  for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+    const int e = static_cast<int>(groups[unit / kMergeUnitsPerGroup]);
+    const int t = (unit / (kBlockM / kMergeRows)) & 1;
+    const int r0 = (unit % (kBlockM / kMergeRows)) * kMergeRows;
+    const SplitEntry en = reinterpret_cast<const SplitEntry*>(split_area)[e];
+    const int nch = en.split & 0xffff;
+    const int seg_end = en.seg_start + en.seg_len;
+    const int row0 = en.q0 + t * kBlockM + r0;
+    if (row0 >= seg_end) continue;  // no rows of the item here (uniform across the CTA)
+    auto slot = [&](int ch) { return parts + (static_cast<size_t>(e + ch) * 2 + t) * kSlot; };
+    __syncthreads();  // the previous unit's weights have been used
+    if (threadIdx.x < kMergeRows) {
+      const int r = threadIdx.x;
+      float l[kSplitMaxChunks];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int ch = 0; ch < kSplitMaxChunks; ++ch) {
+        l[ch] = ch < nch ? slot(ch)[static_cast<size_t>(kBlockM) * D + r0 + r] : -INFINITY;
+        mx = fmaxf(mx, l[ch]);
+      }
+      float den = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < kSplitMaxChunks; ++ch)
+        if (ch < nch) den += __expf(l[ch] - mx);
+      const float lf = mx + logf(den);
+      s_lse[r] = lf;
+#pragma unroll
+      for (int ch = 0; ch < kSplitMaxChunks; ++ch) s_w[r][ch] = ch < nch ? __expf(l[ch] - lf) : 0.f;
+    }
+    __syncthreads();
+    constexpr int kGroups = D / 8;  // 8 columns (16 bytes of output) per thread and step
+    for (int u = threadIdx.x; u < kMergeRows * kGroups; u += kMergeThreads) {
+      const int r = u / kGroups, cg = u % kGroups;
+      const int q_row = row0 + r;
+      if (q_row >= seg_end) continue;
+      float4 x[kSplitMaxChunks][2];
+#pragma unroll
+      for (int ch = 0; ch < kSplitMaxChunks; ++ch) {
+        if (ch < nch) {
+          const float4* src =
+              reinterpret_cast<const float4*>(slot(ch) + static_cast<size_t>(r0 + r) * D + cg * 8);
+          x[ch][0] = src[0];
+          x[ch][1] = src[1];
+        } else {
+          x[ch][0] = x[ch][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ch = 0; ch < kSplitMaxChunks; ++ch) {
+        const float w = s_w[r][ch];
+        acc[0] = fmaf(w, x[ch][0].x, acc[0]);
+        acc[1] = fmaf(w, x[ch][0].y, acc[1]);
+        acc[2] = fmaf(w, x[ch][0].z, acc[2]);
+        acc[3] = fmaf(w, x[ch][0].w, acc[3]);
+        acc[4] = fmaf(w, x[ch][1].x, acc[4]);
+        acc[5] = fmaf(w, x[ch][1].y, acc[5]);
+        acc[6] = fmaf(w, x[ch][1].z, acc[6]);
+        acc[7] = fmaf(w, x[ch][1].w, acc[7]);
+      }
+      *reinterpret_cast<uint4*>(out + (static_cast<size_t>(q_row) * num_heads + en.head) * D + cg * 8) =
+          make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                     pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+      if (lse != nullptr && cg == 0) lse[static_cast<size_t>(en.head) * capacity + q_row] = s_lse[r];
+    }
+  }
+}
+
+// Exclusive prefix sum over the block (kPlanThreads threads) of one value per thread, and the
+// total: a shuffle scan inside each warp, then the warps' totals through shared memory.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* s_warp,
+                                                         uint32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();  // s_warp may still be read from a previous call
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the warps' totals (32 warps), total in the last slot
+    const uint32_t t = s_warp[lane];
+    uint32_t y = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t z = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) y += z;
+    }
+    s_warp[lane] = y - t;
+    if (lane == 31) s_warp[32] = y;
+  }
+  __syncthreads();
+  total = s_warp[32];
+  return s_warp[warp] + x - v;
+}
+
 __global__ void __launch_bounds__(kPlanThreads)
 attn_plan_kernel(const int32_t* __restrict__ cu, int num_segments, int capacity, int max_seqlen,
-                 int num_heads, uint32_t* __restrict__ ws, unsigned int* err) {
+                 int num_heads, uint32_t* __restrict__ ws, uint8_t* __restrict__ split_area,
+                 int wave, unsigned int* err) {
   __shared__ int s_len[kSortMax];
-  __shared__ uint32_t s_part[kPlanThreads];
+  __shared__ uint32_t s_prefix[kSortMax + 1];   // the item prefix again, for the split's lookups
+  __shared__ uint32_t s_warp[kPlanThreads / 32 + 1];
+  __shared__ uint32_t s_ngroups;
   const int S = num_segments;
   const int tid = threadIdx.x;
   uint32_t* order = ws + kWsHeader;
@@ -292,29 +454,113 @@ attn_plan_kernel(const int32_t* __restrict__ cu, int num_segments, int capacity,
   const int lo = min(S, tid * chunk), hi = min(S, lo + chunk);
   uint32_t local = 0;
   for (int i = lo; i < hi; ++i) local += items_of(len_of(static_cast<int>(order[i])), num_heads);
-  s_part[tid] = local;
-  __syncthreads();
-  for (int off = 1; off < kPlanThreads; off <<= 1) {  // inclusive Hillis-Steele scan
-    const uint32_t v = tid >= off ? s_part[tid - off] : 0u;
-    __syncthreads();
-    s_part[tid] += v;
-    __syncthreads();
-  }
-  uint32_t run = tid ? s_part[tid - 1] : 0u;
+  uint32_t total;
+  uint32_t run = block_exclusive_scan(local, s_warp, total);
   for (int i = lo; i < hi; ++i) {
     prefix[i] = run;
+    if (sorted) s_prefix[i] = run;
     run += items_of(len_of(static_cast<int>(order[i])), num_heads);
   }
   if (tid == kPlanThreads - 1) {
-    prefix[S] = s_part[kPlanThreads - 1];
-    ws[1] = s_part[kPlanThreads - 1];
+    prefix[S] = total;
+    if (sorted) s_prefix[S] = total;
+  }
+
+  // ---- the last wave: items [tail, total) -------------------------------------------------
+  const uint32_t tail = wave > 0 ? total / static_cast<uint32_t>(wave) * static_cast<uint32_t>(wave)
+                                 : total;
+  const uint32_t R = total - tail;
+  if (split_area == nullptr || !sorted || R == 0 || R > static_cast<uint32_t>(kSplitMaxEntries) ||
+      R > static_cast<uint32_t>(kPlanThreads) || wave > kSplitMaxWave) {
+    if (tid == 0) {
+      ws[0] = 0;
+      ws[1] = total;
+      ws[2] = total;
+      ws[3] = 0;
+    }
+    return;
+  }
+  __syncthreads();  // prefix complete
+  // thread i < R: whole item tail + i
+  int g = 0, a = 0, len = 0, head = 0, q0 = 0, nkv = 0;
+  if (tid < static_cast<int>(R)) {
+    const uint32_t item = tail + static_cast<uint32_t>(tid);
+    int l = 0, h = S - 1;
+    while (l < h) {
+      const int mid = (l + h + 1) >> 1;
+      if (s_prefix[mid] <= item) l = mid; else h = mid - 1;
+    }
+    g = static_cast<int>(order[l]);
+    len = s_len[g];
+    a = cu[g];
+    const int pairs = (len + kRowsPerItem - 1) / kRowsPerItem;
+    const int loc = static_cast<int>(item - s_prefix[l]);
+    head = loc / pairs;
+    q0 = a + (loc % pairs) * kRowsPerItem;
+    nkv = (len + kBlockN - 1) / kBlockN;
+  }
+  // How many chunks: the L long items of the wave (at least kSplitMinTiles key tiles) are each cut
+  // into c = wave / L chunks (at most kSplitMaxChunks, each of at least 4 key tiles), so that
+  // their chunks about fill one round of the wave's CTAs; the short items follow them round-robin.
+  const bool splittable = tid < static_cast<int>(R) && nkv >= kSplitMinTiles;
+  uint32_t n_long;
+  block_exclusive_scan(splittable ? 1u : 0u, s_warp, n_long);
+  const int c_all = n_long > 0 ? min(kSplitMaxChunks, wave / static_cast<int>(n_long)) : 1;
+  int c = tid < static_cast<int>(R) ? (splittable ? max(1, min(c_all, nkv / 4)) : 1) : 0;
+  uint32_t E;
+  uint32_t first = block_exclusive_scan(static_cast<uint32_t>(c), s_warp, E);
+  if (E > static_cast<uint32_t>(kSplitMaxEntries)) {  // too many chunks for the area: stay whole
+    c = tid < static_cast<int>(R) ? 1 : 0;
+    first = static_cast<uint32_t>(tid);
+    E = R;
+  }
+  SplitEntry* entries = reinterpret_cast<SplitEntry*>(split_area);
+  if (tid == 0) s_ngroups = 0u;
+  __syncthreads();
+  if (c > 1) {  // a split item: list its first entry for the merge (list order is immaterial)
+    const uint32_t gi = atomicAdd(&s_ngroups, 1u);
+    reinterpret_cast<uint32_t*>(split_area + split_groups_offset())[gi] = first;
+  }
+  __syncthreads();
+  for (int ch = 0; ch < c; ++ch) {
+    SplitEntry e;
+    e.seg_start = a;
+    e.seg_len = len;
+    e.head = head;
+    e.q0 = q0;
+    e.kv0 = nkv * ch / c;
+    e.kv1 = nkv * (ch + 1) / c;
+    e.group = static_cast<int>(first);
+    e.split = c > 1 ? (ch << 16 | c) : 0;
+    entries[first + ch] = e;
+  }
+  if (tid == 0) {
+    ws[0] = s_ngroups;
+    ws[1] = tail + E;
+    ws[2] = tail;
+    ws[3] = E;
   }
 }
 
-// Item index -> work descriptor (binary search of the ordered prefix).
+// Item index -> work descriptor: a whole item (binary search of the ordered prefix) or an entry
+// of the split last wave.
 __device__ __forceinline__ WorkDesc decode_item(uint32_t item, const uint32_t* __restrict__ ws,
                                                 const int32_t* __restrict__ cu, int S,
-                                                int num_heads) {
+                                                const uint8_t* __restrict__ split_area) {
+  WorkDesc d;
+  const uint32_t tail = ws[2];
+  if (item >= tail) {
+    const SplitEntry e = reinterpret_cast<const SplitEntry*>(split_area)[item - tail];
+    d.seg_start = e.seg_start;
+    d.seg_len = e.seg_len;
+    d.head = e.head;
+    d.q0 = e.q0;
+    d.pk.kv0 = e.kv0;
+    d.nkv = e.kv1 - e.kv0;
+    d.pk.split = e.split;
+    d.pk.group = e.group;
+    return d;
+  }
   const uint32_t* order = ws + kWsHeader;
   const uint32_t* prefix = ws + kWsHeader + S;
   int lo = 0, hi = S - 1;  // last i with prefix[i] <= item (empty segments repeat a value)
@@ -326,12 +572,14 @@ __device__ __forceinline__ WorkDesc decode_item(uint32_t item, const uint32_t* _
   const int a = cu[g], len = cu[g + 1] - a;
   const uint32_t pairs = static_cast<uint32_t>((len + kRowsPerItem - 1) / kRowsPerItem);
   const uint32_t local = item - prefix[lo];
-  WorkDesc d;
   d.seg_start = a;
   d.seg_len = len;
   d.head = static_cast<int>(local / pairs);
   d.q0 = a + static_cast<int>(local % pairs) * kRowsPerItem;
-  (void)num_heads;
+  d.pk.kv0 = 0;
+  d.nkv = (len + kBlockN - 1) / kBlockN;
+  d.pk.split = 0;
+  d.pk.group = 0;
   return d;
 }
 
@@ -403,7 +651,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 int capacity, int num_heads, float scale, float scale_log2,
                 uint32_t* __restrict__ ws, const __grid_constant__ WindowAttnGeom wg,
                 const uint2* __restrict__ vsa_steps, const int2* __restrict__ vsa_counts,
-                unsigned int* err, unsigned long long wait_ns, unsigned int stall_after) {
+                unsigned int* err, unsigned long long wait_ns, unsigned int stall_after,
+                const uint8_t* __restrict__ split_area) {
   constexpr bool kWin = kMode == kModeWindow;
   constexpr bool kVsa = kMode == kModeVsa;
   using C = Cfg<D, kMode>;
@@ -450,6 +699,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
   // A wait that timed out earlier (recorded, not yet read) means the machinery is not healthy:
   // leave at once instead of running into 2-second waits again.
   if (err != nullptr && *reinterpret_cast<volatile unsigned int*>(err) == kErrTimeout) return;
+  // Packed segments: the grid is sized for the most items the capacity allows; a CTA whose first
+  // item is past the plan's count has nothing to do, and leaves before any set-up.
+  if constexpr (kMode == kModePacked) {
+    if (blockIdx.x >= ws[1]) return;
+  }
 
   // ---- setup: barriers (warp 8), TMEM (warp 9) ----
   if (warp == 8 && lane == 0) {
@@ -558,7 +812,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
             else if constexpr (kVsa)
               d = decode_vsa(item, wg, vsa_counts);
             else
-              d = decode_item(item, ws, cu_seqlens, num_segments, num_heads);
+              d = decode_item(item, ws, cu_seqlens, num_segments, split_area);
           } else {
             d.seg_start = 0;
             d.seg_len = -1;
@@ -618,7 +872,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 stalled = true;
                 break;
               }
-              const int row = d.seg_start + j * kBlockN;
+              const int row = d.seg_start + (d.pk.kv0 + j) * kBlockN;
               const int s = static_cast<int>(kt % SK);
               ok = pwait(bar_kempty(s), ((kt / SK) & 1) ^ 1);
               if (!ok) break;
@@ -1140,6 +1394,31 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
       const float inv_l = 1.f / l;
       __nv_bfloat16* orow = out + (static_cast<size_t>(q_row) * num_heads + d.head) * D;
+      if constexpr (kMode == kModePacked) {
+        if (d.pk.split != 0) {
+          // a chunk of a split item: its partial result (O normalised by its own row sum, and
+          // its LSE) goes to the split area; attn_merge_kernel combines the chunks afterwards
+          constexpr size_t kSlot = static_cast<size_t>(kBlockM) * (D + 1);  // floats per tile
+          float* mine = reinterpret_cast<float*>(const_cast<uint8_t*>(split_area) + split_partials_offset()) +
+                        (static_cast<size_t>(d.pk.group + (d.pk.split >> 16)) * 2 + t) * kSlot;
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t orr[32];
+            tmem_ld32(o_addr + c0, orr);
+            tmem_ld_wait();
+            tmem_reg_fence<32>(orr);
+            float4* dst = reinterpret_cast<float4*>(mine + static_cast<size_t>(row) * D + c0);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              dst[c] = make_float4(__uint_as_float(orr[4 * c]) * inv_l, __uint_as_float(orr[4 * c + 1]) * inv_l,
+                                   __uint_as_float(orr[4 * c + 2]) * inv_l, __uint_as_float(orr[4 * c + 3]) * inv_l);
+          }
+          tc_fence_before();
+          mbar_arrive(bar_oempty(t));
+          mine[static_cast<size_t>(kBlockM) * D + row] = m_used * scale + logf(l);
+          continue;
+        }
+      }
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t orr[32];
@@ -1223,14 +1502,19 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
     want = sms;
   } else {
     attn_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.cu_seqlens, a.num_segments, a.capacity,
-                                                     a.max_seqlen, a.num_heads, ws, a.err);
+                                                     a.max_seqlen, a.num_heads, ws,
+                                                     static_cast<uint8_t*>(a.split_area), sms, a.err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // short segments: one CTA per SM (one fits per SM by shared memory and TMEM) looping over
     // items; long segments: one CTA per item.  Never more CTAs than the largest possible number
     // of items (CTAs past the actual count leave at once).
     max_items = (static_cast<long long>(a.capacity) / kRowsPerItem + a.num_segments) * a.num_heads;
-    want = a.max_seqlen <= kPersistMaxSeqlen ? sms : max_items;
+    // a job of a few waves at most (whose last wave the plan may split) also loops, so that the
+    // short chunks overlap one another's set-up and epilogue
+    const bool short_job = max_items <= static_cast<long long>(kPersistMaxWaves) * sms;
+    if (a.split_area != nullptr) max_items += kSplitMaxEntries;  // chunks of a split last wave
+    want = (a.max_seqlen <= kPersistMaxSeqlen || short_job) ? sms : max_items;
   }
   if (max_items <= 0) return cudaSuccess;
   const int grid = static_cast<int>(max_items < want ? max_items : want);
@@ -1240,8 +1524,17 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
       a.tmap_q, a.tmap_k, a.tmap_v, half ? a.tmap_q2 : a.tmap_q, half ? a.tmap_k2 : a.tmap_k,
       half ? a.tmap_v2 : a.tmap_v, static_cast<__nv_bfloat16*>(a.o), a.lse, a.cu_seqlens,
       a.num_segments, a.capacity, a.num_heads, a.scale, scale_log2, ws, a.wg, a.vsa_steps,
-      a.vsa_counts, a.err, static_cast<unsigned long long>(a.wait_limit_ns), a.stall_after_tiles);
-  return cudaGetLastError();
+      a.vsa_counts, a.err, static_cast<unsigned long long>(a.wait_limit_ns), a.stall_after_tiles,
+      static_cast<const uint8_t*>(a.split_area));
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (kMode == kModePacked && a.split_area != nullptr) {
+    attn_merge_kernel<D><<<4 * sms, kMergeThreads, 0, stream>>>(
+        ws, static_cast<const uint8_t*>(a.split_area), static_cast<__nv_bfloat16*>(a.o), a.lse,
+        a.num_heads, a.capacity);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 }  // namespace

@@ -88,7 +88,8 @@ struct AttnArgs {
   int num_heads;
   int head_dim;
   float scale;
-  void* workspace;  // attn_workspace_bytes(num_segments) bytes: the work plan
+  void* workspace;  // attn_plan_bytes(num_segments) bytes: the work plan
+  void* split_area;  // packed: attn_split_bytes(head_dim) bytes after the plan, or null (no split)
   unsigned int* err;
   uint64_t wait_limit_ns;  // limit of the kernel's pipeline waits (wait_limit_ns() below)
   uint32_t stall_after_tiles;  // testing hook: producers stop after this many K/V tiles
@@ -102,13 +103,27 @@ uint64_t wait_limit_ns();
 // h3_debug_stall_loads changed it).
 uint32_t stall_after_tiles();
 
-// Workspace of the packed variant (uint32 words): [1] total items, [kAttnWsHeaderWords, +S)
-// segment order, [kAttnWsHeaderWords + S, +S+1) exclusive prefix of items in that order; the
-// byte count is rounded up to 256.
+// Workspace of the packed variant.  The plan (uint32 words): [0] split items, [1] work items, [2] whole items
+// before the split last wave, [3] entries of that wave, [kAttnWsHeaderWords, +S) segment order,
+// [kAttnWsHeaderWords + S, +S+1) exclusive prefix of whole items in that order; rounded up to
+// 256 bytes.  Then, optionally, the split area of the last wave (entries, arrival counters and
+// partial results of up to kSplitMaxEntries chunks): with it the call may cut the long items of
+// its last wave into chunks of their key range; without it every item stays whole.
 constexpr int kAttnWsHeaderWords = 4;
-constexpr size_t attn_workspace_bytes(int num_segments) {
+constexpr int kSplitMaxEntries = 320;  // chunks of the last wave (>= 2 x 152 SMs)
+constexpr int kSplitMinSeqlen = 1024;  // the area is only asked for when a segment can be this long
+constexpr size_t attn_plan_bytes(int num_segments) {
   return ((kAttnWsHeaderWords + 2 * static_cast<size_t>(num_segments) + 1) * sizeof(uint32_t) + 255) /
          256 * 256;
+}
+// entries (8 words each), a list of split items (one word each), then per entry and query tile
+// 128 rows of head_dim fp32 values followed by their 128 fp32 LSEs
+constexpr size_t attn_split_bytes(int head_dim) {
+  return static_cast<size_t>(kSplitMaxEntries) * (8 + 1) * sizeof(uint32_t) +
+         static_cast<size_t>(kSplitMaxEntries) * 2 * 128 * (head_dim + 1) * sizeof(float);
+}
+constexpr size_t attn_workspace_bytes(int num_segments, int max_seqlen, int head_dim) {
+  return attn_plan_bytes(num_segments) + (max_seqlen >= kSplitMinSeqlen ? attn_split_bytes(head_dim) : 0);
 }
 cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t stream);
 

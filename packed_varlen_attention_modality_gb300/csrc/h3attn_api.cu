@@ -21,7 +21,7 @@
 // enough for H3_NOALLOC_MAX_SEGMENTS segments) until the process exits.  It is shared by all
 // calls on a device.
 constexpr int kNoallocScratchBytes = 132 * 1024;
-static_assert(h3::attn_workspace_bytes(H3_NOALLOC_MAX_SEGMENTS) <= kNoallocScratchBytes,
+static_assert(h3::attn_plan_bytes(H3_NOALLOC_MAX_SEGMENTS) <= kNoallocScratchBytes,
               "the no-alloc array must hold the plan of H3_NOALLOC_MAX_SEGMENTS segments");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -250,10 +250,8 @@ h3_status h3_rope_apply(const void* q_in, void* q_out, const void* k_in, void* k
 size_t h3_varlen_attn_workspace_size(int32_t num_segments, int32_t num_heads, int32_t max_seqlen,
                                      int32_t head_dim) {
   (void)num_heads;
-  (void)max_seqlen;
-  (void)head_dim;
   if (num_segments <= 0) return 0;
-  return h3::attn_workspace_bytes(num_segments);
+  return h3::attn_workspace_bytes(num_segments, max_seqlen, head_dim);
 }
 
 h3_status h3_varlen_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -272,7 +270,8 @@ h3_status h3_varlen_attn_fwd(const void* q, const void* k, const void* v, void* 
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return H3_ERR_MISALIGNED;
-  const size_t need = h3_varlen_attn_workspace_size(num_segments, num_heads, max_seqlen, head_dim);
+  // the plan is required; the split area after it is used when the workspace holds it
+  const size_t need = num_segments > 0 ? h3::attn_plan_bytes(num_segments) : 0;
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return H3_ERR_WORKSPACE;
   if (workspace != nullptr && !aligned16(workspace)) return H3_ERR_MISALIGNED;
   // work items are counted in 32 bits: (capacity / 256 + segments) * heads must fit
@@ -296,6 +295,8 @@ h3_status h3_varlen_attn_fwd(const void* q, const void* k, const void* v, void* 
   a.head_dim = head_dim;
   a.scale = softmax_scale > 0.f ? softmax_scale : static_cast<float>(1.0 / std::sqrt(head_dim));
   a.workspace = workspace;
+  if (max_seqlen >= h3::kSplitMinSeqlen && workspace_bytes >= need + h3::attn_split_bytes(head_dim))
+    a.split_area = static_cast<uint8_t*>(workspace) + need;
   a.err = device_error_ptr();
   a.wait_limit_ns = h3::wait_limit_ns();
   a.stall_after_tiles = h3::stall_after_tiles();
@@ -320,7 +321,7 @@ h3_status h3_varlen_attn_fwd_noalloc(const void* q, const void* k, const void* v
     return H3_ERR_MISALIGNED;
   // the plan must fit the fixed array: refuse more segments than it was sized for
   if (num_segments > H3_NOALLOC_MAX_SEGMENTS ||
-      h3::attn_workspace_bytes(num_segments) > static_cast<size_t>(kNoallocScratchBytes))
+      h3::attn_plan_bytes(num_segments) > static_cast<size_t>(kNoallocScratchBytes))
     return H3_ERR_WORKSPACE;
   if ((static_cast<int64_t>(capacity) / 256 + num_segments) * num_heads > INT32_MAX)
     return H3_ERR_INVALID_ARG;

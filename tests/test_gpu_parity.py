@@ -238,6 +238,54 @@ def test_maximum_segment_count_against_oracle(h3, dev):
     assert torch.all(o[N:] == 3.0) and torch.all(lse[:, N:] == 5.0)
 
 
+def _split_entries(h3, ws, S, H, D):
+    """(whole items before the last wave, entries of the wave, per-entry chunk field) read back
+    from a workspace after a call: the plan header and the split area's entry table."""
+    plan = h3.varlen_attn_workspace_size(S, H, 1, D)
+    words = ws[:plan].view(torch.int32).cpu().numpy()
+    n = int(words[3])
+    table = ws[plan:plan + 320 * 32].view(torch.int32).cpu().numpy().reshape(320, 8)
+    return int(words[2]), n, table[:n, 7]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("lengths,heads", [([8192], 2),            # fewer items than SMs: all split
+                                           ([3000, 40, 2500], 3),
+                                           ([1024] * 5 + [5000, 1], 1),
+                                           ([2000, 700], 8),       # one CTA per SM, looping
+                                           ([3520, 256, 320], 24)])  # the 4,096-token request's shape
+def test_split_last_wave_against_oracle_and_whole_items(h3, dev, D, lengths, heads):
+    """Long items of the last, partly filled wave are cut into chunks of their key range and
+    merged (a workspace with the split area) -- against the oracle, against the same call with a
+    plan-only workspace (whole items), and bit-identical call after call (fixed merge order)."""
+    wl = W.random_packed(200 + len(lengths) + heads + D, lengths, heads=heads, head_dim=D,
+                         capacity=sum(lengths) + 40)
+    d = _to(dev, wl)
+    S, N = wl.num_segments, wl.num_tokens
+    full = torch.empty(h3.varlen_attn_workspace_size(S, heads, wl.max_seqlen, D), dtype=torch.uint8, device=dev)
+    plan = torch.empty(h3.varlen_attn_workspace_size(S, heads, 1, D), dtype=torch.uint8, device=dev)
+    outs = []
+    for ws in (full, full, plan):
+        o = torch.full_like(d["q"], 3.0)
+        lse = torch.full((heads, wl.capacity), 5.0, device=dev)
+        h3.varlen_attn_fwd(d["q"], d["k"], d["v"], d["cu"], wl.max_seqlen, out=o, lse=lse, workspace=ws)
+        torch.cuda.synchronize()
+        assert h3.get_device_error(dev) == 0
+        outs.append((o, lse))
+        if ws is full:
+            _, n, split = _split_entries(h3, full, S, heads, D)
+            assert n > 0 and np.any(split != 0), "the last wave was expected to split"
+    (o1, l1), (o2, l2), (ow, lw) = outs
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)  # deterministic merge
+    assert torch.all(o1[N:] == 3.0) and torch.all(l1[:, N:] == 5.0)
+    rows = _sample_rows(wl.cu_seqlens, seed=D + heads)
+    ref_o, ref_lse = oracle.varlen_attention(wl.q, wl.k, wl.v, wl.cu_seqlens, rows=rows)
+    for o, lse, what in ((o1, l1, "split"), (ow, lw, "whole")):
+        _close(o[rows].float().cpu().numpy(), ref_o[rows], f"{what} {lengths} x {heads} D {D}")
+        _lse_close(lse[:, rows].cpu().numpy(), ref_lse[:, rows], f"{what} {lengths} x {heads} D {D}")
+    _close(o1[:N].float().cpu().numpy(), ow[:N].float().cpu().numpy(), f"split vs whole {lengths}")
+
+
 def test_explicit_softmax_scale(h3, dev):
     wl = W.random_packed(7, [300, 45], heads=2, head_dim=128)
     d = _to(dev, wl)

@@ -3,9 +3,9 @@
 Some callers cannot allocate device memory -- their memory is owned by an external pool or
 allocator, or a cudaMalloc there would stall or is not allowed -- so the library offers this
 variant that keeps its work plan in a fixed array of its own.  It runs the same plan kernel and
-the same attention kernel as h3_varlen_attn_fwd with a caller workspace, so on the same inputs
-its outputs must be the same bytes, call after call: the shared array keeps the previous call's
-plan, which must never leak into the next one.
+the same attention kernel as h3_varlen_attn_fwd given a workspace that holds the plan alone (no
+room to split the last wave), so on the same inputs its outputs must be the same bytes, call after
+call: the shared array keeps the previous call's plan, which must never leak into the next one.
 
 Kept in a file of its own that pytest collects last.
 """
@@ -57,9 +57,11 @@ def _case(dev, wl):
 
 
 def _with_workspace(lib, dev, c):
+    """The workspace entry point with the plan alone (the size returned for a max_seqlen below
+    1024): like the no-alloc entry point, it then runs every work item whole."""
     o = torch.full_like(c["q"], 5.0)
     lse = torch.full((c["H"], c["C"]), 5.0, device=dev)
-    nbytes = lib.h3_varlen_attn_workspace_size(c["S"], c["H"], c["maxs"], c["D"])
+    nbytes = lib.h3_varlen_attn_workspace_size(c["S"], c["H"], 1, c["D"])
     ws = torch.empty(max(16, nbytes), dtype=torch.uint8, device=dev)
     st = lib.h3_varlen_attn_fwd(_p(c["q"]), _p(c["k"]), _p(c["v"]), _p(o), _p(lse), _p(c["cu"]), c["S"],
                                 c["maxs"], c["C"], c["H"], c["D"], 0.0, _p(ws), nbytes, _stream(dev))
