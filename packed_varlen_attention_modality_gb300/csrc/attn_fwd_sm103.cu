@@ -61,6 +61,7 @@
 #include <atomic>
 
 #include <type_traits>
+#include <utility>
 
 #include "h3_internal.h"
 #include "sm103_ptx.cuh"
@@ -315,6 +316,7 @@ attn_merge_kernel(const uint32_t* __restrict__ ws, const uint8_t* __restrict__ s
                   int capacity) {
   __shared__ float s_w[kMergeRows][kSplitMaxChunks];  // per row: chunk weights exp(lse_c - lse)
   __shared__ float s_lse[kMergeRows];
+  grid_dependency_wait();  // the attention kernel's partial results
   const int n_units = static_cast<int>(ws[0]) * kMergeUnitsPerGroup;
   const uint32_t* groups = reinterpret_cast<const uint32_t*>(split_area + split_groups_offset());
   constexpr size_t kSlot = static_cast<size_t>(kBlockM) * (D + 1);
@@ -425,6 +427,8 @@ attn_plan_kernel(const int32_t* __restrict__ cu, int num_segments, int capacity,
   __shared__ uint32_t s_prefix[kSortMax + 1];   // the item prefix again, for the split's lookups
   __shared__ uint32_t s_warp[kPlanThreads / 32 + 1];
   __shared__ uint32_t s_ngroups;
+  grid_dependency_wait();  // cu_seqlens may come from the kernel before this one
+  launch_dependents();     // the attention kernel may be scheduled now; it waits for this plan
   const int S = num_segments;
   const int tid = threadIdx.x;
   uint32_t* order = ws + kWsHeader;
@@ -696,6 +700,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
   // out and the kernel unwinds.  Every wait still ends (by its limit) and no access changes.
   bool stalled = false;
 
+  // Everything below reads what earlier kernels wrote (Q/K/V, the plan, the error word).
+  grid_dependency_wait();
+  launch_dependents();  // the merge kernel may be scheduled; it waits for this kernel to end
   // A wait that timed out earlier (recorded, not yet read) means the machinery is not healthy:
   // leave at once instead of running into 2-second waits again.
   if (err != nullptr && *reinterpret_cast<volatile unsigned int*>(err) == kErrTimeout) return;
@@ -1459,6 +1466,25 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
   }
 }
 
+// Launch with programmatic stream serialization: the kernel may be scheduled while the previous
+// kernel in the stream finishes (it calls grid_dependency_wait() before reading that kernel's
+// results), which hides the launch latency between the plan, attention and merge kernels.
+template <typename... Params, typename... Args>
+cudaError_t launch_programmatic(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t stream, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 int num_sms_of_current_device() {
   static std::atomic<int> cached[64];  // 0 until looked up; racing lookups store the same value
   int dev = 0;
@@ -1501,9 +1527,10 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
     max_items = (nblk + 3) / 4 * a.num_heads;
     want = sms;
   } else {
-    attn_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.cu_seqlens, a.num_segments, a.capacity,
-                                                     a.max_seqlen, a.num_heads, ws,
-                                                     static_cast<uint8_t*>(a.split_area), sms, a.err);
+    e = launch_programmatic(attn_plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, a.cu_seqlens,
+                            a.num_segments, a.capacity, a.max_seqlen, a.num_heads, ws,
+                            static_cast<uint8_t*>(a.split_area), sms, a.err);
+    if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // short segments: one CTA per SM (one fits per SM by shared memory and TMEM) looping over
@@ -1520,20 +1547,19 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
   const int grid = static_cast<int>(max_items < want ? max_items : want);
   const float scale_log2 = a.scale * 1.4426950408889634f;
   const bool half = kMode == kModeWindow && a.wg.half_h;  // the half-height maps were built
-  attn_fwd_kernel<D, kMode><<<grid, kThreads, C::kSmemBytes, stream>>>(
-      a.tmap_q, a.tmap_k, a.tmap_v, half ? a.tmap_q2 : a.tmap_q, half ? a.tmap_k2 : a.tmap_k,
+  e = launch_programmatic(
+      attn_fwd_kernel<D, kMode>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, a.tmap_q,
+      a.tmap_k, a.tmap_v, half ? a.tmap_q2 : a.tmap_q, half ? a.tmap_k2 : a.tmap_k,
       half ? a.tmap_v2 : a.tmap_v, static_cast<__nv_bfloat16*>(a.o), a.lse, a.cu_seqlens,
-      a.num_segments, a.capacity, a.num_heads, a.scale, scale_log2, ws, a.wg, a.vsa_steps,
-      a.vsa_counts, a.err, static_cast<unsigned long long>(a.wait_limit_ns), a.stall_after_tiles,
-      static_cast<const uint8_t*>(a.split_area));
-  e = cudaGetLastError();
+      a.num_segments, a.capacity, a.num_heads, a.scale, scale_log2, static_cast<uint32_t*>(ws),
+      a.wg, a.vsa_steps, a.vsa_counts, a.err, static_cast<unsigned long long>(a.wait_limit_ns),
+      a.stall_after_tiles, static_cast<const uint8_t*>(a.split_area));
   if (e != cudaSuccess) return e;
-  if (kMode == kModePacked && a.split_area != nullptr) {
-    attn_merge_kernel<D><<<4 * sms, kMergeThreads, 0, stream>>>(
-        ws, static_cast<const uint8_t*>(a.split_area), static_cast<__nv_bfloat16*>(a.o), a.lse,
-        a.num_heads, a.capacity);
-    e = cudaGetLastError();
-  }
+  if (kMode == kModePacked && a.split_area != nullptr)
+    e = launch_programmatic(attn_merge_kernel<D>, dim3(4 * sms), dim3(kMergeThreads), 0, stream,
+                            static_cast<const uint32_t*>(ws),
+                            static_cast<const uint8_t*>(a.split_area),
+                            static_cast<__nv_bfloat16*>(a.o), a.lse, a.num_heads, a.capacity);
   return e;
 }
 

@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 
 #include "h3_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace h3 {
 namespace {
@@ -53,6 +54,9 @@ rope_kernel(const uint4* q_in, uint4* q_out, const uint4* k_in, uint4* k_out,
             int num_requests, const float* __restrict__ start_frames,
             const __grid_constant__ RopeTables tab) {
   __shared__ float2 cs[kTokens][kMaxPairs];
+  // Nothing of what this kernel writes (Q and K) is read by the plan kernel that may follow it:
+  // let that kernel be scheduled now (it waits for this grid before reading anything).
+  launch_dependents();
   const int tok0 = blockIdx.x * kTokens;
   const int ntok = min(kTokens, num_tokens - tok0);
   const int P = head_dim >> 1;

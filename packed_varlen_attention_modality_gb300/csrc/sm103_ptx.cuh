@@ -81,6 +81,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic stream serialization
+// attribute may begin while the kernel before it in the stream is still running; it must call
+// grid_dependency_wait() before touching anything that kernel writes (the wait returns once that
+// kernel has completed and its memory operations are visible; at once without the attribute).
+// launch_dependents() lets the next such kernel be scheduled before this one ends.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Order this thread's generic-proxy shared-memory writes before later async-proxy accesses
 // (TMA, tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
