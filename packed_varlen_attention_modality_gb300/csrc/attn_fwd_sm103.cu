@@ -286,7 +286,6 @@ __device__ __forceinline__ uint32_t items_of(int len, int heads) {
 // rows of D fp32 values followed by their 128 fp32 LSEs.
 constexpr int kSplitMinTiles = 8;   // split only items of at least 8 key tiles (1,024 keys)
 constexpr int kSplitMaxChunks = 8;
-constexpr int kSplitMaxWave = 256;  // the split is planned for grids of at most this many CTAs
 struct SplitEntry {
   int seg_start, seg_len, head, q0, kv0, kv1, group, split;  // split = chunk << 16 | chunks
 };
@@ -475,7 +474,7 @@ attn_plan_kernel(const int32_t* __restrict__ cu, int num_segments, int capacity,
                                  : total;
   const uint32_t R = total - tail;
   if (split_area == nullptr || !sorted || R == 0 || R > static_cast<uint32_t>(kSplitMaxEntries) ||
-      R > static_cast<uint32_t>(kPlanThreads) || wave > kSplitMaxWave) {
+      R > static_cast<uint32_t>(kPlanThreads)) {
     if (tid == 0) {
       ws[0] = 0;
       ws[1] = total;
