@@ -248,6 +248,40 @@ def _split_entries(h3, ws, S, H, D):
     return int(words[2]), n, table[:n, 7]
 
 
+def _expected_split_plan(cu, H, sms):
+    """The plan's split of the last wave, restated on the host: segments longest first (ties by
+    position), items head-major per segment, whole items [0, tail) with tail a multiple of the SM
+    count, then the last wave's entries (seg_start, seg_len, head, q0, kv0, kv1, group, split):
+    each of its L long items (>= 8 key tiles) cut into min(8, SMs // L, key tiles // 4) chunks."""
+    lens = np.diff(np.asarray(cu, np.int64))
+    order = sorted(range(len(lens)), key=lambda g: (-lens[g], g))
+    items = []
+    for g in order:
+        pairs = -(-int(lens[g]) // 256)
+        for h in range(H):
+            for p in range(pairs):
+                items.append((int(cu[g]), int(lens[g]), h, int(cu[g]) + 256 * p))
+    T = len(items)
+    tail = T // sms * sms
+    R = T - tail
+    if R == 0 or R > 320:
+        return tail if R == 0 else T, []
+    wave = items[tail:]
+    nkv = [-(-ln // 128) for (_, ln, _, _) in wave]
+    L = sum(1 for x in nkv if x >= 8)
+    c_all = min(8, sms // L) if L else 1
+    cs = [max(1, min(c_all, x // 4)) if x >= 8 else 1 for x in nkv]
+    if sum(cs) > 320:
+        cs = [1] * R
+    entries, first = [], 0
+    for (a, ln, h, q0), x, c in zip(wave, nkv, cs):
+        for ch in range(c):
+            entries.append((a, ln, h, q0, x * ch // c, x * (ch + 1) // c, first,
+                            (ch << 16 | c) if c > 1 else 0))
+        first += c
+    return tail, entries
+
+
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("lengths,heads", [([8192], 2),            # fewer items than SMs: all split
                                            ([3000, 40, 2500], 3),
@@ -273,8 +307,15 @@ def test_split_last_wave_against_oracle_and_whole_items(h3, dev, D, lengths, hea
         assert h3.get_device_error(dev) == 0
         outs.append((o, lse))
         if ws is full:
-            _, n, split = _split_entries(h3, full, S, heads, D)
+            tail, n, split = _split_entries(h3, full, S, heads, D)
             assert n > 0 and np.any(split != 0), "the last wave was expected to split"
+            # the entry table, integer for integer, against the rule restated on the host
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            exp_tail, exp_entries = _expected_split_plan(wl.cu_seqlens, heads, sms)
+            plan_bytes = h3.varlen_attn_workspace_size(S, heads, 1, D)
+            table = full[plan_bytes:plan_bytes + 320 * 32].view(torch.int32).cpu().numpy().reshape(320, 8)
+            assert tail == exp_tail and n == len(exp_entries)
+            assert np.array_equal(table[:n], np.asarray(exp_entries, np.int32).reshape(-1, 8))
     (o1, l1), (o2, l2), (ow, lw) = outs
     assert torch.equal(o1, o2) and torch.equal(l1, l2)  # deterministic merge
     assert torch.all(o1[N:] == 3.0) and torch.all(l1[:, N:] == 5.0)
