@@ -318,6 +318,10 @@ def test_split_last_wave_against_oracle_and_whole_items(h3, dev, D, lengths, hea
             assert np.array_equal(table[:n], np.asarray(exp_entries, np.int32).reshape(-1, 8))
     (o1, l1), (o2, l2), (ow, lw) = outs
     assert torch.equal(o1, o2) and torch.equal(l1, l2)  # deterministic merge
+    o_nolse = torch.full_like(d["q"], 3.0)  # the merge without an LSE output writes the same rows
+    h3.varlen_attn_fwd(d["q"], d["k"], d["v"], d["cu"], wl.max_seqlen, out=o_nolse, workspace=full)
+    torch.cuda.synchronize()
+    assert torch.equal(o_nolse, o1)
     assert torch.all(o1[N:] == 3.0) and torch.all(l1[:, N:] == 5.0)
     rows = _sample_rows(wl.cu_seqlens, seed=D + heads)
     ref_o, ref_lse = oracle.varlen_attention(wl.q, wl.k, wl.v, wl.cu_seqlens, rows=rows)
