@@ -703,8 +703,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
   grid_dependency_wait();
   launch_dependents();  // the merge kernel may be scheduled; it waits for this kernel to end
   // A wait that timed out earlier (recorded, not yet read) means the machinery is not healthy:
-  // leave at once instead of running into 2-second waits again.
-  if (err != nullptr && *reinterpret_cast<volatile unsigned int*>(err) == kErrTimeout) return;
+  // leave at once instead of running into 2-second waits again.  The threads decide together, so
+  // that a timeout recorded by another CTA meanwhile cannot send some of them on to the set-up
+  // barrier without the others.
+  if (__syncthreads_or(err != nullptr &&
+                       *reinterpret_cast<volatile unsigned int*>(err) == kErrTimeout))
+    return;
   // Packed segments: the grid is sized for the most items the capacity allows; a CTA whose first
   // item is past the plan's count has nothing to do, and leaves before any set-up.
   if constexpr (kMode == kModePacked) {

@@ -287,7 +287,9 @@ def _expected_split_plan(cu, H, sms):
                                            ([3000, 40, 2500], 3),
                                            ([1024] * 5 + [5000, 1], 1),
                                            ([2000, 700], 8),       # one CTA per SM, looping
-                                           ([3520, 256, 320], 24)])  # the 4,096-token request's shape
+                                           ([3520, 256, 320], 24),  # the 4,096-token request's shape
+                                           ([1100] * 31 + [40], 1),  # 32 segments: the wave crosses two
+                                           ([1100] * 40, 1)])        # more: planned by the plan kernel
 def test_split_last_wave_against_oracle_and_whole_items(h3, dev, D, lengths, heads):
     """Long items of the last, partly filled wave are cut into chunks of their key range and
     merged (a workspace with the split area) -- against the oracle, against the same call with a
@@ -315,6 +317,13 @@ def test_split_last_wave_against_oracle_and_whole_items(h3, dev, D, lengths, hea
             plan_bytes = h3.varlen_attn_workspace_size(S, heads, 1, D)
             table = full[plan_bytes:plan_bytes + 320 * 32].view(torch.int32).cpu().numpy().reshape(320, 8)
             assert tail == exp_tail and n == len(exp_entries)
+            # the order and item-prefix words: longest first, ties by position
+            words = full[:plan_bytes].view(torch.int32).cpu().numpy()
+            lens = np.diff(wl.cu_seqlens.astype(np.int64))
+            order = sorted(range(S), key=lambda g: (-lens[g], g))
+            items = [-(-int(lens[g]) // 256) * heads for g in order]
+            assert words[4:4 + S].tolist() == order
+            assert words[4 + S:5 + 2 * S].tolist() == [0] + np.cumsum(items).tolist()
             assert np.array_equal(table[:n], np.asarray(exp_entries, np.int32).reshape(-1, 8))
     (o1, l1), (o2, l2), (ow, lw) = outs
     assert torch.equal(o1, o2) and torch.equal(l1, l2)  # deterministic merge
