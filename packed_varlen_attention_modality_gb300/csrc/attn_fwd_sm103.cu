@@ -312,10 +312,13 @@ template <int D>
 __global__ void __launch_bounds__(kMergeThreads)
 attn_merge_kernel(const uint32_t* __restrict__ ws, const uint8_t* __restrict__ split_area,
                   __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int num_heads,
-                  int capacity) {
+                  int capacity, const unsigned int* err) {
   __shared__ float s_w[kMergeRows][kSplitMaxChunks];  // per row: chunk weights exp(lse_c - lse)
   __shared__ float s_lse[kMergeRows];
   grid_dependency_wait();  // the attention kernel's partial results
+  // After a timeout (in that kernel or recorded before it) the partials are incomplete or stale:
+  // merge nothing, so that a launch made while the error is recorded leaves the output untouched.
+  if (err != nullptr && *reinterpret_cast<const volatile unsigned int*>(err) == kErrTimeout) return;
   const int n_units = static_cast<int>(ws[0]) * kMergeUnitsPerGroup;
   const uint32_t* groups = reinterpret_cast<const uint32_t*>(split_area + split_groups_offset());
   constexpr size_t kSlot = static_cast<size_t>(kBlockM) * (D + 1);
@@ -1562,7 +1565,8 @@ cudaError_t launch(const AttnArgs& a, cudaStream_t stream) {
     e = launch_programmatic(attn_merge_kernel<D>, dim3(4 * sms), dim3(kMergeThreads), 0, stream,
                             static_cast<const uint32_t*>(ws),
                             static_cast<const uint8_t*>(a.split_area),
-                            static_cast<__nv_bfloat16*>(a.o), a.lse, a.num_heads, a.capacity);
+                            static_cast<__nv_bfloat16*>(a.o), a.lse, a.num_heads, a.capacity,
+                            a.err);
   return e;
 }
 
