@@ -219,6 +219,54 @@ def test_edge_lengths_against_oracle(h3, dev, D, lengths):
     assert torch.all(o[N:] == 3.0) and torch.all(lse[:, N:] == 5.0)
 
 
+def _random_layout(seed):
+    """A seeded random job: 1-47 segments whose lengths mix empty and tiny ones, lengths at and
+    around multiples of the 128-row tile, and long ones up to 4,000 rows; 1-8 heads."""
+    rng = np.random.default_rng(seed)
+    S = int(rng.integers(1, 48))
+    lengths = []
+    for _ in range(S):
+        kind = rng.random()
+        if kind < 0.35:
+            lengths.append(int(rng.integers(0, 41)))
+        elif kind < 0.7:
+            lengths.append(max(0, 128 * int(rng.integers(1, 12)) + int(rng.integers(-2, 3))))
+        else:
+            lengths.append(int(rng.integers(41, 4001)))
+    while sum(lengths) > 14000:
+        lengths[int(np.argmax(lengths))] //= 2
+    heads = int(rng.choice([1, 2, 3, 5, 8]))
+    return lengths, heads, int(rng.integers(0, 200))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("seed", range(8))
+def test_random_layouts_against_oracle(h3, dev, D, seed):
+    """Seeded random segment layouts through the library's default workspace (which splits the
+    last wave when it can): every valid row and its LSE against the oracle, pad rows untouched,
+    and the same bytes from a second call."""
+    lengths, heads, pad = _random_layout(1000 + seed)
+    wl = W.random_packed(1100 + seed + D, lengths, heads=heads, head_dim=D, capacity=sum(lengths) + pad + 1)
+    d = _to(dev, wl)
+    outs = []
+    for _ in range(2):
+        o = torch.full_like(d["q"], 3.0)
+        lse = torch.full((heads, wl.capacity), 5.0, device=dev)
+        h3.varlen_attn_fwd(d["q"], d["k"], d["v"], d["cu"], max(1, wl.max_seqlen), out=o, lse=lse)
+        torch.cuda.synchronize()
+        assert h3.get_device_error(dev) == 0
+        outs.append((o, lse))
+    (o, lse), (o2, lse2) = outs
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    N = wl.num_tokens
+    what = f"seed {seed} D {D}: {len(lengths)} segments, max {max(lengths)}, {heads} heads"
+    if N:
+        ref_o, ref_lse = oracle.varlen_attention(wl.q, wl.k, wl.v, wl.cu_seqlens)
+        _close(o[:N].float().cpu().numpy(), ref_o[:N], what)
+        _lse_close(lse[:, :N].cpu().numpy(), ref_lse[:, :N], what)
+    assert torch.all(o[N:] == 3.0) and torch.all(lse[:, N:] == 5.0), what
+
+
 def test_maximum_segment_count_against_oracle(h3, dev):
     """65,535 segments (the most the call accepts) of 0 to 4 rows each: the plan lists far more
     segments than it orders longest-first, most items hold a single short query tile, and the
@@ -546,6 +594,48 @@ def test_window_attention_in_place_small_grids_full_oracle(h3, dev, D, grid, win
     ref_lse_orig[:, perm] = ref_lse
     _close(o.float().cpu().numpy(), ref_o, f"in place {grid} {win} {shift} D {D}")
     _lse_close(lse.cpu().numpy(), ref_lse_orig, f"in place {grid} {win} {shift} D {D}")
+
+
+def _random_window_geometry(seed):
+    """A seeded random grid and a supported window (height x width dividing 128, at most 256
+    tokens) with a random shift: edge windows cropped on every side, windows wider than the grid."""
+    rng = np.random.default_rng(seed)
+    while True:
+        win = (int(rng.choice([1, 2, 3, 4])), int(rng.choice([1, 2, 4, 8])), int(rng.choice([1, 2, 4, 8, 16, 32, 64])))
+        if 128 % (win[1] * win[2]) == 0 and win[0] * win[1] * win[2] <= 256 and win[1] * win[2] >= 4:
+            break
+    grid = (int(rng.integers(1, 10)), int(rng.integers(1, 21)), int(rng.integers(1, 41)))
+    shift = tuple(int(rng.integers(0, w)) for w in win)
+    return grid, win, shift
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("seed", range(6))
+def test_window_random_geometries_against_oracle(h3, dev, D, seed):
+    """Seeded random grids, windows and shifts: the partition (perm and cu_seqlens) bit-exact, the
+    packed rows exact, and attention in place on every row against the oracle."""
+    grid, win, shift = _random_window_geometry(2000 + seed)
+    n = grid[0] * grid[1] * grid[2]
+    rng = np.random.default_rng(2100 + seed + D)
+    q, k, v = (torch.from_numpy(rng.standard_normal((n, 2, D)).astype(np.float32)).to(torch.bfloat16)
+               for _ in range(3))
+    what = f"grid {grid} win {win} shift {shift} D {D}"
+    perm_ref, cu_ref = oracle.window_partition(grid, win, shift)
+    perm, cu, packed = h3.window_pack(grid, win, shift, [q.to(dev)])
+    torch.cuda.synchronize()
+    assert np.array_equal(perm.cpu().numpy(), perm_ref), what
+    assert np.array_equal(cu.cpu().numpy(), cu_ref), what
+    assert torch.equal(packed[0].cpu(), oracle.window_pack(q, perm_ref)), what
+    o, lse = h3.window_attn_fwd(q.to(dev), k.to(dev), v.to(dev), grid, win, shift, return_lse=True)
+    torch.cuda.synchronize()
+    assert h3.get_device_error(dev) == 0
+    ref_o, ref_lse = oracle.varlen_attention(oracle.window_pack(q, perm_ref), oracle.window_pack(k, perm_ref),
+                                             oracle.window_pack(v, perm_ref), cu_ref)
+    ref_o = oracle.window_unpack(ref_o, perm_ref)
+    ref_lse_orig = np.empty_like(ref_lse)
+    ref_lse_orig[:, perm_ref] = ref_lse
+    _close(o.float().cpu().numpy(), ref_o, what)
+    _lse_close(lse.cpu().numpy(), ref_lse_orig, what)
 
 
 def test_cuda_graph_replay_is_bit_identical_to_eager(h3, dev):
